@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of the retention core on one B300 (or N replicas, one per GPU).
+
+Headline workload (the one `value` reports): chunkwise recurrent retention,
+long sequence -- b1 H16 N32768 dk256 dv512 chunk 256, bf16 Q/K/V ~ N(0,1)/16,
+fp32 state, fp32 output.  A step is one full chunkwise forward over that
+batch (intra-chunk products, cross-chunk read, state update; decay masks made
+in registers).  The same JSON line also reports the decode workload (512
+recurrent steps at b128 H16 dk256 dv512, fp32 state) and the parallel form
+with all three normalisations and the GroupNorm/swish epilogue (b8 H8 N2048),
+each with its own roofline.
+
+Timing: W warm-up steps, then K steps between CUDA events on the launching
+stream, bracketed by a barrier and synchronisation; inputs are larger than L2
+(126 MB) so no flush is needed.  Multi-GPU (torchrun): independent replicas,
+one per GPU, weak scaling; the elapsed time is the max over ranks.
+
+`--impl reference` times the fp64 CPU oracle (the only reference this project
+has) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_recurrence_sequence_chunkwise_b300 import inputs  # noqa: E402
+
+METRIC = ("retention fwd tokens/s & % tensor peak (chunkwise); decode tokens/s & HBM GB/s")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------------------- dist
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend: str | None = None):
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+        return self
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        """Max of a scalar over ranks (timing only; no data-path collective)."""
+        if self.pg is None:
+            return x
+        dev = "cuda" if torch.cuda.is_available() and self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate(dist: Dist, elapsed_ms: float, units_per_rank: float) -> tuple[float, float]:
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    worst = dist.max(elapsed_ms)
+    return units_per_rank * dist.world / (worst / 1e3), worst
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ret_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if re.match(r"^[\d.]+$", r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def profile_traffic(summary_name: str, source_file: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the kernel
+    source changed since the counters were taken (the summary records its hash)."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_hash and m_bytes):
+        return None
+    src = os.path.join(ROOT, "linear_recurrence_sequence_chunkwise_b300", "csrc", source_file)
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m_bytes.group(1)) if cur == m_hash.group(1) else None
+
+
+def timed(fn, steps: int, warmup: int, dist: Dist, stream=None, counter=None):
+    """W untimed steps, then K steps between CUDA events on the launching stream.
+    Returns (elapsed ms of this rank, counter delta over the timed steps)."""
+    stream = stream or torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0 = counter() if counter else 0
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    c1 = counter() if counter else 0
+    torch.cuda.synchronize()
+    dist.barrier()
+    return e0.elapsed_time(e1), c1 - c0
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_chunkwise_sample(w, tokens: int, threads: int):
+    """Oracle chunkwise on `threads` heads x `tokens` tokens of workload w, one head
+    per host thread.  Returns (tokens/s, seconds, description)."""
+    import oracle
+    heads = threads
+    q, k, v = inputs.qkv(inputs.Workload("sample", 1, heads, tokens, w.dk, w.dv, w.dtype,
+                                         w.scale, chunk=w.chunk, seed=w.seed + 77))
+    gam = inputs.gammas(w.H)[:heads] if heads <= w.H else (inputs.gammas(w.H) * 8)[:heads]
+
+    def unit(h):
+        return oracle.chunkwise(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], [gam[h]], w.chunk)
+
+    oracle.default()
+    t0 = time.perf_counter()
+    oracle.map_units(unit, range(heads), threads)
+    dt = time.perf_counter() - t0
+    desc = (f"{heads} heads x {tokens} tokens of {w.name} (dk{w.dk} dv{w.dv} chunk {w.chunk}), "
+            f"fp64 oracle, one head per host thread")
+    return heads * tokens / dt, dt, desc
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return 0
+    w = inputs.CHUNKWISE_LONG
+    threads = max(1, min(os.cpu_count() or 1, w.H))
+    tokens = 2048
+    for _ in range(args.warmup):
+        oracle_chunkwise_sample(w, tokens, threads)
+    total, tps = 0.0, []
+    for _ in range(args.steps):
+        r, dt, desc = oracle_chunkwise_sample(w, tokens, threads)
+        total += dt
+        tps.append(r)
+    value = args.steps * threads * tokens / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, "f32"),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def workload_config(w, out_dtype: str):
+    return {"workload": f"{w.name}: chunkwise retention b{w.b} H{w.H} N{w.N} dk{w.dk} dv{w.dv} "
+                        f"chunk {w.chunk}, {w.dtype} q/k/v N(0,1)/sqrt(dk), fp32 state, "
+                        f"{out_dtype} out, gamma_h = 1-2^(-5-h)",
+            "b": w.b, "H": w.H, "N": w.N, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+            "out_dtype": out_dtype,
+            "l2": "inputs (1.07 GB) larger than L2 (126 MB); no flush between steps"}
+
+
+def bench_chunkwise(args, dist, rb, pk, out_dtype):
+    w = inputs.CHUNKWISE_LONG
+    q, k, v = inputs.qkv(w, "cuda")
+    od = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    o = torch.empty(w.b, w.H, w.N, w.dv, dtype=od, device="cuda")
+    fn = lambda: rb.retention_chunkwise(q, k, v, w.gamma, w.chunk, out=o)  # noqa: E731
+    with Clocks(torch.cuda.current_device()) as clk:
+        ms, launches = timed(fn, args.steps, args.warmup, dist, counter=rb.kernel_launches)
+    rb.check_device_error()
+    tokens = w.b * w.N
+    value, worst = aggregate(dist, ms, tokens * args.steps)
+    flops = inputs.algorithmic_flops("chunkwise", w)
+    ms_step = worst / args.steps
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    in_bytes = 2 * (2 * w.b * w.H * w.N * w.dk + w.b * w.H * w.N * w.dv)
+    out_bytes = w.b * w.H * w.N * w.dv * (4 if out_dtype == "f32" else 2)
+    traffic = profile_traffic(f"chunkwise_tc_{w.name}.md", "tc_chunkwise.cu")
+    res = {"value": value, "ms_per_step": ms_step, "launches": launches,
+           "clocks": clk.summary(),
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": traffic,
+                        "algorithmic_flops_per_launch": flops,
+                        "algorithmic_bytes_per_launch": in_bytes + out_bytes,
+                        "achieved_gbs": (in_bytes + out_bytes) / (ms_step * 1e-3) / 1e9}}
+    # end to end through the public API with host buffers: H2D of q, k, v from
+    # pinned memory, the call, D2H of the output, every step.
+    hq, hk, hv = (t.to("cpu").pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        rb.retention_chunkwise(q, k, v, w.gamma, w.chunk, out=o)
+        ho.copy_(o, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    ms_e2e, _ = timed(e2e_step, e2e_steps, 1, dist)
+    e2e_val, _ = aggregate(dist, ms_e2e, tokens * e2e_steps)
+    res["e2e"] = {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": in_bytes,
+                  "d2h_bytes_per_step": out_bytes}
+    del q, k, v, o, hq, hk, hv, ho
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(args, dist, rb, pk):
+    w = inputs.DECODE
+    state = inputs.decode_state(w, "cuda")
+    qs, ks, vs = inputs.decode_all_inputs(w, "cuda")
+    o = torch.empty(w.b, w.H, w.dv, dtype=torch.float32, device="cuda")
+
+    def run_all():
+        for t in range(w.steps):
+            rb.retention_recurrent_step(qs[t], ks[t], vs[t], state, w.gamma, out=o)
+
+    ms, _ = timed(run_all, 1, 1, dist)
+    rb.check_device_error()
+    ms_step = ms / w.steps
+    tokens = w.b * w.steps
+    value, _ = aggregate(dist, ms, tokens)
+    state_bytes = 2 * 4 * w.b * w.H * w.dk * w.dv
+    io_bytes = 2 * w.b * w.H * (2 * w.dk + w.dv) + 4 * w.b * w.H * w.dv
+    gbs = (state_bytes + io_bytes) / (ms_step * 1e-3) / 1e9
+    del state, qs, ks, vs, o
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: b{w.b} H{w.H} dk{w.dk} dv{w.dv}, {w.steps} steps, fp32 state "
+                        f"N(0,0.1^2), bf16 q/k/v N(0,1)/16, fp32 out",
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": profile_traffic("decode_decode.md", "decode.cu"),
+                         "algorithmic_bytes_per_launch": state_bytes + io_bytes}}
+
+
+def bench_parallel(args, dist, rb, pk):
+    w = inputs.PARALLEL_NORM
+    q, k, v = inputs.qkv(w, "cuda")
+    g = inputs.gate(w, "cuda")
+    y = torch.empty(w.b, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+    out = torch.empty(w.b, w.N, w.H * w.dv, dtype=torch.float32, device="cuda")
+
+    def step():
+        rb.retention_parallel(q, k, v, w.gamma, w.flags, out=y)
+        rb.msr_epilogue(y, g, w.eps, out=out)
+
+    steps = max(3, args.steps // 2)
+    ms, _ = timed(step, steps, max(1, args.warmup // 2), dist)
+    rb.check_device_error()
+    ms_step = ms / steps
+    tokens = w.b * w.N
+    value, _ = aggregate(dist, ms, tokens * steps)
+    flops = inputs.algorithmic_flops("parallel", w)
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    del q, k, v, g, y, out
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: b{w.b} H{w.H} N{w.N} dk{w.dk} dv{w.dv}, bf16 in, all three "
+                        "normalisations, GroupNorm(eps 1e-5)+swish gate epilogue, fp32 out",
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "traffic": profile_traffic(f"parallel_tc_{w.name}.md", "tc_parallel.cu"),
+                         "algorithmic_flops_per_launch": flops}}
+
+
+def cpu_baseline_leg():
+    w = inputs.CHUNKWISE_LONG
+    threads = max(1, min(os.cpu_count() or 1, w.H))
+    tps, dt, desc = oracle_chunkwise_sample(w, 8192, threads)
+    return {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": desc + f" ({dt:.1f} s wall)"}
+
+
+def run_ours(args, dist: Dist):
+    from linear_recurrence_sequence_chunkwise_b300 import binding as rb
+    rb.lib()
+    pk, pk_src = peaks()
+    out_dtype = args.out_dtype
+    main = bench_chunkwise(args, dist, rb, pk, out_dtype)
+    extra = {}
+    if not args.only_headline:
+        extra["decode"] = bench_decode(args, dist, rb, pk)
+        extra["parallel"] = bench_parallel(args, dist, rb, pk)
+    cpu = cpu_baseline_leg() if (dist.rank == 0 and dist.world == 1 and not args.no_cpu) else None
+    if dist.rank != 0:
+        return 0
+    w = inputs.CHUNKWISE_LONG
+    line = {"metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(w, out_dtype),
+            "roofline": main["roofline"], "peak_source": f"{pk_src} (MEASURED_PEAKS.json burst)"
+            if pk_src == "measured" else "fallback",
+            "cpu_baseline": cpu, "e2e": main["e2e"], "gpu_launches": main["launches"],
+            "clocks": main["clocks"]}
+    line.update(extra)
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--only-headline", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, dist)
+    dist.init()
+    try:
+        return run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

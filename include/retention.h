@@ -1,0 +1,145 @@
+/*
+ * retention.h -- C ABI of the RetNet multi-scale retention core on one NVIDIA
+ * B300 (sm_103a).  Library: libretention_b300.so (hand-written CUDA kernels).
+ *
+ * Sources for what each call computes (page title, then section / equation):
+ *   [RN2] "Transformer取代者登場！微軟、清華剛推出RetNet：成本低、速度快、性能強（2）"
+ *         "Retention" 1) parallel form eq.(5), 2) recurrent form eq.(6),
+ *         3) chunkwise recurrent form eq.(7); "門控多尺度 Retention" (per-head
+ *         decay, GroupNorm per head, swish gate); "Retention Score 歸一化"
+ *         (three score normalisations); "訓練/推理" (eqs.5/7 for training,
+ *         eq.6 for decoding).
+ *   [RVW] "[論文レビュー] Retentive Network: A Successor to Transformer for Large
+ *         Language Models", ABSTRACT (three computation paradigms).
+ *
+ * Notation: b batch, H heads, N sequence length, dk key/query head dim, dv
+ * value head dim, B chunk length, gamma_h the fixed decay of head h.  Indices
+ * are 0-based.  Q and K arrive already position-rotated (the xPos factor of
+ * [RN2] eqs.(2)-(3) is absorbed into them); inputs are real, so the conjugate
+ * transpose of eq.(4) is a transpose.
+ *
+ * Common rules for every call
+ *   - Pointers named q, k, v, o, y, g, out, state, state_in, state_out are
+ *     DEVICE pointers to contiguous row-major arrays, 16-byte aligned.  The
+ *     caller owns every buffer; the library allocates nothing.
+ *   - gamma is a HOST pointer to H doubles, each in [0, 1].
+ *   - Calls are asynchronous on the CUDA stream `stream` (a cudaStream_t; NULL
+ *     means the legacy default stream).  Argument checks run on the host
+ *     before any launch: a rejected call launches nothing and leaves every
+ *     output untouched.  A launch failure returns RET_ERR_CUDA.  Nothing
+ *     throws across the ABI.
+ *   - Sizes of zero (b, H or N) are valid and launch nothing.
+ *   - Supported shapes: 1 <= H <= 128; dk and dv multiples of 16 with
+ *     dk <= 256 and dv <= 512; chunk a multiple of 16 in [16, 256] dividing N.
+ *     Other values return RET_ERR_UNSUPPORTED (dims, H) or RET_ERR_SHAPE
+ *     (chunk / N mismatch, negative sizes).
+ *   - Outputs are written in out_dtype (RET_F32 or RET_BF16, round to nearest
+ *     even); all accumulation is fp32; recurrent states are always fp32.
+ *   - Kernels that wait on on-chip barriers bound every wait; if one gives up
+ *     it records the fact in a device-side error word and the kernel returns
+ *     early.  retention_check_device_error() reads (and clears) that word.
+ */
+#ifndef RETENTION_B300_H
+#define RETENTION_B300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RET_OK = 0,
+    RET_ERR_NULL = 1,        /* a required pointer is NULL                      */
+    RET_ERR_SHAPE = 2,       /* negative size, N % chunk != 0, bad chunk        */
+    RET_ERR_DTYPE = 3,       /* dtype code not RET_F32 / RET_BF16               */
+    RET_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned                */
+    RET_ERR_UNSUPPORTED = 5, /* dims/heads/flags/gamma/eps outside the support  */
+    RET_ERR_CUDA = 6,        /* a CUDA launch or runtime call failed            */
+    RET_ERR_TIMEOUT = 7      /* a bounded on-chip wait expired inside a kernel  */
+} ret_status;
+
+typedef enum { RET_F32 = 0, RET_BF16 = 1 } ret_dtype;
+
+/* Score normalisations of [RN2] "Retention Score 歸一化" (parallel form only). */
+#define RET_NORM_SCALE 1u  /* scores q_n.k_m divided by sqrt(dk)                 */
+#define RET_NORM_DECAY 2u  /* row n of D divided by sqrt(sum_m D[n][m])          */
+#define RET_NORM_ROWSUM 4u /* row n of the scores R divided by max(|sum_m R|, 1) */
+
+/*
+ * Parallel form, [RN2] "Retention" 1) eq.(5) with Fig.3a, plus the optional
+ * normalisations of "Retention Score 歸一化":
+ *   D[n][m]  = gamma_h^(n-m) for n >= m, else 0        (never materialised)
+ *   R[n][m]  = (q_n . k_m) [/ sqrt(dk)] * D[n][m] [/ sqrt(sum_i D[n][i])]
+ *   R[n][.] /= max(|sum_m R[n][m]|, 1)                  (RET_NORM_ROWSUM)
+ *   O        = R V
+ * q, k: [b][H][N][dk] in in_dtype; v: [b][H][N][dv] in in_dtype;
+ * o: [b][H][N][dv] in out_dtype (written).  flags: OR of RET_NORM_*.
+ */
+int retention_parallel(const void* q, const void* k, const void* v, void* o,
+                       ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                       int dk, int dv, const double* gamma, unsigned flags, void* stream);
+
+/*
+ * Chunkwise recurrent form, [RN2] "Retention" 3) eq.(7): parallel inside each
+ * chunk of length B = chunk, recurrent across chunks.  For chunk i (rows
+ * iB..iB+B-1; j, r index rows inside the chunk):
+ *   O[iB+j] = sum_{r<=j} (q_j . k_r) gamma^(j-r) v_r + gamma^(j+1) (q_j R_{i-1})
+ *   R_i     = sum_r gamma^(B-1-r) k_r^T v_r + gamma^B R_{i-1}
+ * R_{-1} = state_in (NULL means zero).  If state_out is not NULL it receives
+ * the final state R_{N/B-1}; state_in and state_out may alias.
+ * q, k: [b][H][N][dk]; v: [b][H][N][dv] (in_dtype); o: [b][H][N][dv] (out_dtype);
+ * state_in, state_out: [b][H][dk][dv] fp32.  No score normalisation.
+ * Requires N % chunk == 0 (RET_ERR_SHAPE otherwise).
+ */
+int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
+                        ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                        int dk, int dv, int chunk, const double* gamma,
+                        const float* state_in, float* state_out, void* stream);
+
+/*
+ * One decode step of the recurrent form, [RN2] "Retention" 2) eq.(6) and the
+ * inference paragraph of "訓練/推理" (O(1) state per token):
+ *   S <- gamma_h S + k^T v     (in place, fp32)
+ *   o  = q S                   (read from the UPDATED state)
+ * q, k: [b][H][dk]; v: [b][H][dv] (in_dtype); state: [b][H][dk][dv] fp32, read
+ * and overwritten; o: [b][H][dv] (out_dtype).  dv must be a multiple of 16.
+ */
+int retention_recurrent_step(const void* q, const void* k, const void* v, float* state,
+                             void* o, ret_dtype in_dtype, ret_dtype out_dtype, int b, int H,
+                             int dk, int dv, const double* gamma, void* stream);
+
+/*
+ * Gated multi-scale retention epilogue, [RN2] "門控多尺度 Retention":
+ *   per (batch, token n, head h): mu, var = mean and biased variance of the dv
+ *   values y[b][h][n][:];  yhat = (y - mu) / sqrt(var + eps) [* weight + bias];
+ *   out[b][n][h*dv + c] = swish(g[b][n][h*dv + c]) * yhat[c],  swish(x) = x sigmoid(x).
+ * y: [b][H][N][dv] (y_dtype, head-major as the retention calls write it);
+ * g, out: [b][N][H*dv] (token-major like X W_G); weight, bias: H*dv floats on
+ * the DEVICE, each nullable (identity).  eps >= 0.  The output projection W_O
+ * is not part of this call.
+ */
+int msr_epilogue(const void* y, const void* g, void* out, ret_dtype y_dtype,
+                 ret_dtype g_dtype, ret_dtype out_dtype, int b, int H, int N, int dv,
+                 float eps, const float* weight, const float* bias, void* stream);
+
+/* Static text for a ret_status code ("unknown status" for other values). */
+const char* retention_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side error word of
+ * the current device.  Returns RET_ERR_TIMEOUT if any kernel since the last
+ * check gave up on a bounded wait, RET_ERR_CUDA if the synchronisation itself
+ * failed, RET_OK otherwise.
+ */
+int retention_check_device_error(void* stream);
+
+/*
+ * Number of kernels this library has launched in this process so far (all
+ * devices, all calls).  Host-side counter, incremented after each successful
+ * launch; lets callers count launches inside a timed region.
+ */
+unsigned long long retention_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RETENTION_B300_H */

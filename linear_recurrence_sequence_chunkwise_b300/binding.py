@@ -1,0 +1,185 @@
+"""Thin ctypes binding of include/retention.h (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of libretention_b300.so;
+this module only turns torch tensors into device pointers, sizes, dtype codes
+and a stream handle, and turns non-zero status codes into exceptions.  It
+fails loudly if the library is missing: there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libretention_b300.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "retention.h")
+
+RET_OK, RET_ERR_NULL, RET_ERR_SHAPE, RET_ERR_DTYPE, RET_ERR_ALIGN = 0, 1, 2, 3, 4
+RET_ERR_UNSUPPORTED, RET_ERR_CUDA, RET_ERR_TIMEOUT = 5, 6, 7
+RET_F32, RET_BF16 = 0, 1
+NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
+NORM_ALL = 7
+
+_lib = None
+_lock = threading.Lock()
+
+
+class RetentionError(RuntimeError):
+    def __init__(self, func: str, status: int, text: str):
+        super().__init__(f"{func}: status {status} ({text})")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/retention.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decl = r"^(?:const\s+)?(?:unsigned\s+)?(?:long\s+)*\w+\s*\**\s+\**(\w+)\s*\("
+    return re.findall(decl, text, flags=re.M)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libretention_b300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python linear_recurrence_sequence_chunkwise_b300/build.py`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, u, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float
+            dp = ctypes.POINTER(ctypes.c_double)
+            L.retention_parallel.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, dp, u, vp]
+            L.retention_chunkwise.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp, vp, vp, vp]
+            L.retention_recurrent_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, dp, vp]
+            L.msr_epilogue.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, vp]
+            L.retention_status_string.argtypes = [i]
+            L.retention_status_string.restype = ctypes.c_char_p
+            L.retention_check_device_error.argtypes = [vp]
+            L.retention_kernel_launches.argtypes = []
+            L.retention_kernel_launches.restype = ctypes.c_ulonglong
+            for name in ("retention_parallel", "retention_chunkwise", "retention_recurrent_step",
+                         "msr_epilogue", "retention_check_device_error"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().retention_status_string(status).decode()
+
+
+def _check(func: str, rc: int):
+    if rc != RET_OK:
+        raise RetentionError(func, rc, status_string(rc))
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return RET_F32
+    if t == torch.bfloat16:
+        return RET_BF16
+    raise TypeError(f"unsupported dtype {t}; use torch.float32 or torch.bfloat16")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _gamma(gamma, H: int):
+    g = [float(x) for x in gamma]
+    if len(g) != H:
+        raise ValueError(f"gamma has {len(g)} entries, expected H={H}")
+    return (ctypes.c_double * max(H, 1))(*g)
+
+
+def retention_parallel(q, k, v, gamma, flags: int = 0, out=None, out_dtype=torch.float32,
+                       stream=None):
+    """Parallel form (eq.5) with optional normalisation flags.  q,k:[b,H,N,dk] v:[b,H,N,dv]."""
+    b, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((b, H, N, dv), dtype=out_dtype, device=q.device)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    rc = lib().retention_parallel(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _dtype_code(q.dtype),
+                                  _dtype_code(out.dtype), b, H, N, dk, dv, _gamma(gamma, H),
+                                  flags, _stream(stream))
+    _check("retention_parallel", rc)
+    return out
+
+
+def retention_chunkwise(q, k, v, gamma, chunk: int, state_in=None, state_out=None, out=None,
+                        out_dtype=torch.float32, stream=None):
+    """Chunkwise recurrent form (eq.7).  state_in/state_out: fp32 [b,H,dk,dv] or None."""
+    b, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((b, H, N, dv), dtype=out_dtype, device=q.device)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    for s in (state_in, state_out):
+        if s is not None and s.dtype != torch.float32:
+            raise TypeError("states are fp32")
+    rc = lib().retention_chunkwise(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _dtype_code(q.dtype),
+                                   _dtype_code(out.dtype), b, H, N, dk, dv, chunk,
+                                   _gamma(gamma, H), _ptr(state_in), _ptr(state_out),
+                                   _stream(stream))
+    _check("retention_chunkwise", rc)
+    return out
+
+
+def retention_recurrent_step(q, k, v, state, gamma, out=None, out_dtype=torch.float32,
+                             stream=None):
+    """One decode step (eq.6), state updated in place.  q,k:[b,H,dk] v:[b,H,dv]."""
+    b, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((b, H, dv), dtype=out_dtype, device=q.device)
+    if state.dtype != torch.float32:
+        raise TypeError("the state is fp32")
+    rc = lib().retention_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(state), _ptr(out),
+                                        _dtype_code(q.dtype), _dtype_code(out.dtype), b, H, dk,
+                                        dv, _gamma(gamma, H), _stream(stream))
+    _check("retention_recurrent_step", rc)
+    return out
+
+
+def msr_epilogue(y, g, eps: float = 1e-5, weight=None, bias=None, out=None,
+                 out_dtype=torch.float32, stream=None):
+    """GroupNorm per (token, head) + swish(G) gate.  y:[b,H,N,dv] g:[b,N,H*dv]."""
+    b, H, N, dv = y.shape
+    if out is None:
+        out = torch.empty((b, N, H * dv), dtype=out_dtype, device=y.device)
+    rc = lib().msr_epilogue(_ptr(y), _ptr(g), _ptr(out), _dtype_code(y.dtype),
+                            _dtype_code(g.dtype), _dtype_code(out.dtype), b, H, N, dv,
+                            float(eps), _ptr(weight), _ptr(bias), _stream(stream))
+    _check("msr_epilogue", rc)
+    return out
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process (host-side counter)."""
+    return int(lib().retention_kernel_launches())
+
+
+def check_device_error(stream=None):
+    """Synchronise and raise if a kernel gave up on a bounded wait."""
+    _check("retention_check_device_error", lib().retention_check_device_error(_stream(stream)))

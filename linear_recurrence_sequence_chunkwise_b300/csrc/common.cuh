@@ -1,0 +1,94 @@
+// common.cuh -- shared types and small device helpers of the retention library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/retention.h"
+
+namespace ret {
+
+constexpr int kMaxHeads = 128;
+
+// Per-head decay constants, computed on the host in fp64 and rounded once.
+//   l2g  = log2(gamma)            (-inf for gamma = 0)
+//   lng  = ln(gamma)              (-inf for gamma = 0)
+//   omg  = 1 - gamma
+//   gB   = gamma^B                (chunkwise only; gamma^1 elsewhere)
+//   g1   = gamma
+struct HeadConsts {
+    float g1[kMaxHeads];
+    float l2g[kMaxHeads];
+    float lng[kMaxHeads];
+    float omg[kMaxHeads];
+    float gB[kMaxHeads];
+};
+
+// gamma^e for an integer exponent e >= 0 from log2(gamma): exp2(e * log2 gamma),
+// with gamma = 0 handled exactly (0^0 = 1, 0^e = 0).
+__device__ __forceinline__ float decay_pow(float l2g, float e) {
+    if (e == 0.0f) return 1.0f;
+    return exp2f(e * l2g);  // l2g = -inf -> 0
+}
+
+// Row sum of D, s_n = sum_{i<=n} gamma^(n-i) = (1 - gamma^(n+1)) / (1 - gamma),
+// written with expm1 so that gamma close to 1 keeps full precision.
+__device__ __forceinline__ float decay_rowsum(float lng, float omg, int n) {
+    if (omg == 0.0f) return (float)(n + 1);          // gamma = 1
+    if (isinf(lng)) return 1.0f;                      // gamma = 0
+    return -expm1f((float)(n + 1) * lng) / omg;
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return *p; }
+    static __device__ __forceinline__ void store(float* p, float x) { *p = x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+};
+
+template <typename T> __device__ __forceinline__ float ld(const T* p) { return Elem<T>::load(p); }
+template <typename T> __device__ __forceinline__ void st(T* p, float x) { Elem<T>::store(p, x); }
+
+}  // namespace ret
+
+// Host-side launchers implemented by the kernel files (all return cudaError_t
+// of the launch; argument checks have already passed).
+namespace ret {
+cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v, float* state,
+                                  void* o, int in_bf16, int out_bf16, int b, int H, int dk,
+                                  int dv, const HeadConsts& hc, cudaStream_t s);
+cudaError_t launch_msr_epilogue(const void* y, const void* g, void* out, int y_bf16,
+                                int g_bf16, int out_bf16, int b, int H, int N, int dv,
+                                float eps, const float* weight, const float* bias,
+                                cudaStream_t s);
+cudaError_t launch_parallel_simt(const void* q, const void* k, const void* v, void* o,
+                                 int in_bf16, int out_bf16, int b, int H, int N, int dk, int dv,
+                                 const HeadConsts& hc, unsigned flags, cudaStream_t s);
+cudaError_t launch_chunkwise_simt(const void* q, const void* k, const void* v, void* o,
+                                  int in_bf16, int out_bf16, int b, int H, int N, int dk,
+                                  int dv, int chunk, const HeadConsts& hc,
+                                  const float* state_in, float* state_out, cudaStream_t s);
+// Tensor-core paths: return cudaErrorNotSupported when the shape is outside
+// what the kernel handles, so the caller can pick the CUDA-core kernel.
+cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, void* o,
+                                int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
+                                const HeadConsts& hc, const float* state_in, float* state_out,
+                                cudaStream_t s);
+cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
+                               int out_bf16, int b, int H, int N, int dk, int dv,
+                               const HeadConsts& hc, unsigned flags, cudaStream_t s);
+// Count one successful kernel launch (host-side, process-wide).
+void count_launch();
+// Device error words of the kernels with bounded waits: read and clear.
+unsigned read_clear_error_tc_chunkwise(cudaStream_t s);
+unsigned read_clear_error_tc_parallel(cudaStream_t s);
+}  // namespace ret

@@ -1,0 +1,176 @@
+// retention_abi.cu -- the C ABI of include/retention.h: argument checks, per-head
+// constants, kernel selection.  Host code only; kernels live in the other files.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+using ret::HeadConsts;
+
+namespace ret {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace ret
+
+namespace {
+
+bool is_dtype(int d) { return d == RET_F32 || d == RET_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dims_ok(int dk, int dv) {
+    return dk > 0 && dv > 0 && dk % 16 == 0 && dv % 16 == 0 && dk <= 256 && dv <= 512;
+}
+
+// Decay constants of each head in fp64, rounded to fp32 once.  gamma must lie
+// in [0, 1] ([RN2] "門控多尺度 Retention": a fixed decay per head).
+int head_consts(const double* gamma, int H, int B, HeadConsts* hc) {
+    if (H > ret::kMaxHeads) return RET_ERR_UNSUPPORTED;
+    memset(hc, 0, sizeof(*hc));
+    for (int h = 0; h < H; ++h) {
+        double g = gamma[h];
+        if (!(g >= 0.0 && g <= 1.0)) return RET_ERR_UNSUPPORTED;  // also rejects NaN
+        hc->l2g[h] = (g == 0.0) ? -INFINITY : (float)log2(g);
+        hc->lng[h] = (g == 0.0) ? -INFINITY : (float)log(g);
+        hc->omg[h] = (float)(1.0 - g);
+        hc->g1[h] = (float)g;
+        hc->gB[h] = (float)pow(g, (double)B);
+    }
+    return RET_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? RET_OK : RET_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* retention_status_string(int status) {
+    switch (status) {
+        case RET_OK: return "ok";
+        case RET_ERR_NULL: return "a required pointer is NULL";
+        case RET_ERR_SHAPE: return "invalid shape (negative size, or N not a multiple of a valid chunk)";
+        case RET_ERR_DTYPE: return "dtype code is neither RET_F32 nor RET_BF16";
+        case RET_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case RET_ERR_UNSUPPORTED: return "unsupported dims, heads, flags, gamma or eps";
+        case RET_ERR_CUDA: return "CUDA launch or runtime error";
+        case RET_ERR_TIMEOUT: return "a bounded on-chip wait expired inside a kernel";
+        default: return "unknown status";
+    }
+}
+
+int retention_parallel(const void* q, const void* k, const void* v, void* o,
+                       ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N, int dk,
+                       int dv, const double* gamma, unsigned flags, void* stream) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (flags & ~(RET_NORM_SCALE | RET_NORM_DECAY | RET_NORM_ROWSUM)) return RET_ERR_UNSUPPORTED;
+    if (!dims_ok(dk, dv)) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || H == 0 || N == 0) return RET_OK;
+    if (!q || !k || !v || !o || !gamma) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RET_ERR_ALIGN;
+    HeadConsts hc;
+    int rc = head_consts(gamma, H, 1, &hc);
+    if (rc != RET_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int ob = out_dtype == RET_BF16;
+    if (in_dtype == RET_BF16) {
+        cudaError_t e = ret::launch_parallel_tc(q, k, v, o, ob, b, H, N, dk, dv, hc, flags, s);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    return cuda_status(ret::launch_parallel_simt(q, k, v, o, in_dtype == RET_BF16, ob, b, H, N,
+                                                 dk, dv, hc, flags, s));
+}
+
+int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
+                        ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N, int dk,
+                        int dv, int chunk, const double* gamma, const float* state_in,
+                        float* state_out, void* stream) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (!dims_ok(dk, dv)) return RET_ERR_UNSUPPORTED;
+    if (chunk < 16 || chunk > 256 || chunk % 16 != 0) return RET_ERR_SHAPE;
+    if (N % chunk != 0) return RET_ERR_SHAPE;
+    if (b == 0 || H == 0) return RET_OK;
+    if (!gamma) return RET_ERR_NULL;
+    if (N == 0) {
+        // No tokens: the final state is the incoming one.
+        if (!state_out) return RET_OK;
+        if (!aligned16(state_out) || (state_in && !aligned16(state_in))) return RET_ERR_ALIGN;
+        size_t bytes = (size_t)b * H * dk * dv * sizeof(float);
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (state_in) {
+            if (state_in == state_out) return RET_OK;
+            return cuda_status(cudaMemcpyAsync(state_out, state_in, bytes,
+                                               cudaMemcpyDeviceToDevice, s));
+        }
+        return cuda_status(cudaMemsetAsync(state_out, 0, bytes, s));
+    }
+    if (!q || !k || !v || !o) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RET_ERR_ALIGN;
+    if ((state_in && !aligned16(state_in)) || (state_out && !aligned16(state_out)))
+        return RET_ERR_ALIGN;
+    HeadConsts hc;
+    int rc = head_consts(gamma, H, chunk, &hc);
+    if (rc != RET_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int ob = out_dtype == RET_BF16;
+    if (in_dtype == RET_BF16) {
+        cudaError_t e = ret::launch_chunkwise_tc(q, k, v, o, ob, b, H, N, dk, dv, chunk, hc,
+                                                 state_in, state_out, s);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    return cuda_status(ret::launch_chunkwise_simt(q, k, v, o, in_dtype == RET_BF16, ob, b, H, N,
+                                                  dk, dv, chunk, hc, state_in, state_out, s));
+}
+
+int retention_recurrent_step(const void* q, const void* k, const void* v, float* state, void* o,
+                             ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int dk,
+                             int dv, const double* gamma, void* stream) {
+    if (b < 0 || H < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (!dims_ok(dk, dv)) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || H == 0) return RET_OK;
+    if (!q || !k || !v || !state || !o || !gamma) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o))
+        return RET_ERR_ALIGN;
+    HeadConsts hc;
+    int rc = head_consts(gamma, H, 1, &hc);
+    if (rc != RET_OK) return rc;
+    return cuda_status(ret::launch_recurrent_step(q, k, v, state, o, in_dtype == RET_BF16,
+                                                  out_dtype == RET_BF16, b, H, dk, dv, hc,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+int msr_epilogue(const void* y, const void* g, void* out, ret_dtype y_dtype, ret_dtype g_dtype,
+                 ret_dtype out_dtype, int b, int H, int N, int dv, float eps,
+                 const float* weight, const float* bias, void* stream) {
+    if (b < 0 || H < 0 || N < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(y_dtype) || !is_dtype(g_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (dv <= 0 || dv % 16 != 0 || dv > 512) return RET_ERR_UNSUPPORTED;
+    if (H > ret::kMaxHeads) return RET_ERR_UNSUPPORTED;
+    if (!(eps >= 0.0f) || isinf(eps)) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || H == 0 || N == 0) return RET_OK;
+    if (!y || !g || !out) return RET_ERR_NULL;
+    if (!aligned16(y) || !aligned16(g) || !aligned16(out)) return RET_ERR_ALIGN;
+    if ((weight && !aligned16(weight)) || (bias && !aligned16(bias))) return RET_ERR_ALIGN;
+    return cuda_status(ret::launch_msr_epilogue(y, g, out, y_dtype == RET_BF16,
+                                                g_dtype == RET_BF16, out_dtype == RET_BF16, b, H,
+                                                N, dv, eps, weight, bias,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+unsigned long long retention_kernel_launches(void) { return ret::g_launches.load(); }
+
+int retention_check_device_error(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RET_ERR_CUDA;
+    unsigned e = ret::read_clear_error_tc_chunkwise(s) | ret::read_clear_error_tc_parallel(s);
+    if (cudaGetLastError() != cudaSuccess) return RET_ERR_CUDA;
+    return e ? RET_ERR_TIMEOUT : RET_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI (no GPU needed; no call here reaches a launch).
+
+The library must load, export every function include/retention.h declares,
+and reject bad arguments with the documented status codes before touching the
+GPU.  Fake pointers are never dereferenced: every call below fails validation.
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from linear_recurrence_sequence_chunkwise_b300 import binding, build
+
+A = ctypes.c_void_p(0x100000)       # 16-byte aligned, never dereferenced
+A2 = ctypes.c_void_p(0x200000)
+MIS = ctypes.c_void_p(0x100004)     # not 16-byte aligned
+NUL = None
+S = ctypes.c_void_p(0)              # default stream handle, never used here
+
+
+def G(*vals):
+    return (ctypes.c_double * len(vals))(*vals)
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return binding.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = binding.header_functions()
+    assert set(names) == {"retention_parallel", "retention_chunkwise", "retention_recurrent_step",
+                          "msr_epilogue", "retention_status_string",
+                          "retention_check_device_error", "retention_kernel_launches"}
+    for n in names:
+        assert getattr(L, n) is not None
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+
+
+def test_launch_counter_starts_at_zero_and_rejections_do_not_count(L):
+    before = binding.kernel_launches()
+    assert par(L, dk=24) == binding.RET_ERR_UNSUPPORTED
+    assert binding.kernel_launches() == before
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert binding.status_string(code)
+    assert binding.status_string(99) == "unknown status"
+    assert binding.status_string(0) == "ok"
+
+
+def par(L, q=A, k=A, v=A, o=A2, it=1, ot=0, b=1, H=2, N=64, dk=64, dv=64, g=None, flags=0):
+    g = G(0.9, 0.5) if g is None else g
+    return L.retention_parallel(q, k, v, o, it, ot, b, H, N, dk, dv, g, flags, S)
+
+
+def chk(L, q=A, k=A, v=A, o=A2, it=1, ot=0, b=1, H=2, N=64, dk=64, dv=64, chunk=16, g=None,
+        si=None, so=None):
+    g = G(0.9, 0.5) if g is None else g
+    return L.retention_chunkwise(q, k, v, o, it, ot, b, H, N, dk, dv, chunk, g, si, so, S)
+
+
+def dec(L, q=A, k=A, v=A, st=A2, o=A2, it=1, ot=0, b=1, H=2, dk=64, dv=64, g=None):
+    g = G(0.9, 0.5) if g is None else g
+    return L.retention_recurrent_step(q, k, v, st, o, it, ot, b, H, dk, dv, g, S)
+
+
+def epi(L, y=A, g=A, o=A2, yt=0, gt=1, ot=0, b=1, H=2, N=8, dv=64, eps=1e-5, w=None, bias=None):
+    return L.msr_epilogue(y, g, o, yt, gt, ot, b, H, N, dv, ctypes.c_float(eps), w, bias, S)
+
+
+def test_parallel_rejections(L):
+    assert par(L, b=-1) == binding.RET_ERR_SHAPE
+    assert par(L, N=-3) == binding.RET_ERR_SHAPE
+    assert par(L, it=2) == binding.RET_ERR_DTYPE
+    assert par(L, ot=-1) == binding.RET_ERR_DTYPE
+    assert par(L, flags=8) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, dk=24) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, dk=512) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, dv=528) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, q=NUL) == binding.RET_ERR_NULL
+    assert par(L, g=ctypes.POINTER(ctypes.c_double)()) == binding.RET_ERR_NULL
+    assert par(L, v=MIS) == binding.RET_ERR_ALIGN
+    assert par(L, o=MIS) == binding.RET_ERR_ALIGN
+    assert par(L, g=G(0.9, 1.5)) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, g=G(-0.1, 0.5)) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, g=G(float("nan"), 0.5)) == binding.RET_ERR_UNSUPPORTED
+    assert par(L, H=129, g=G(*([0.5] * 129))) == binding.RET_ERR_UNSUPPORTED
+
+
+def test_empty_inputs_launch_nothing(L):
+    assert par(L, b=0, q=NUL, k=NUL, v=NUL, o=NUL) == binding.RET_OK
+    assert par(L, N=0, q=NUL, k=NUL, v=NUL, o=NUL) == binding.RET_OK
+    assert par(L, H=0, q=NUL, k=NUL, v=NUL, o=NUL, g=G(0.5)) == binding.RET_OK
+    assert chk(L, b=0, q=NUL, k=NUL, v=NUL, o=NUL) == binding.RET_OK
+    assert chk(L, N=0, q=NUL, k=NUL, v=NUL, o=NUL) == binding.RET_OK   # no state_out: nothing to do
+    assert dec(L, b=0, q=NUL, k=NUL, v=NUL, st=NUL, o=NUL) == binding.RET_OK
+    assert epi(L, N=0, y=NUL, g=NUL, o=NUL) == binding.RET_OK
+
+
+def test_chunkwise_rejections(L):
+    assert chk(L, chunk=8) == binding.RET_ERR_SHAPE
+    assert chk(L, chunk=24) == binding.RET_ERR_SHAPE
+    assert chk(L, chunk=512, N=512) == binding.RET_ERR_SHAPE
+    assert chk(L, N=100) == binding.RET_ERR_SHAPE
+    assert chk(L, N=64, chunk=48) == binding.RET_ERR_SHAPE
+    assert chk(L, it=5) == binding.RET_ERR_DTYPE
+    assert chk(L, dv=8) == binding.RET_ERR_UNSUPPORTED
+    assert chk(L, k=NUL) == binding.RET_ERR_NULL
+    assert chk(L, si=MIS) == binding.RET_ERR_ALIGN
+    assert chk(L, so=MIS) == binding.RET_ERR_ALIGN
+    assert chk(L, g=G(0.9, 1.01)) == binding.RET_ERR_UNSUPPORTED
+
+
+def test_recurrent_step_rejections(L):
+    assert dec(L, st=NUL) == binding.RET_ERR_NULL
+    assert dec(L, o=MIS) == binding.RET_ERR_ALIGN
+    assert dec(L, dk=0) == binding.RET_ERR_UNSUPPORTED
+    assert dec(L, dk=-16) == binding.RET_ERR_SHAPE
+    assert dec(L, it=3) == binding.RET_ERR_DTYPE
+    assert dec(L, g=G(0.5, 2.0)) == binding.RET_ERR_UNSUPPORTED
+
+
+def test_epilogue_rejections(L):
+    assert epi(L, eps=-1.0) == binding.RET_ERR_UNSUPPORTED
+    assert epi(L, eps=float("inf")) == binding.RET_ERR_UNSUPPORTED
+    assert epi(L, eps=float("nan")) == binding.RET_ERR_UNSUPPORTED
+    assert epi(L, dv=520) == binding.RET_ERR_UNSUPPORTED
+    assert epi(L, dv=24) == binding.RET_ERR_UNSUPPORTED
+    assert epi(L, gt=9) == binding.RET_ERR_DTYPE
+    assert epi(L, y=NUL) == binding.RET_ERR_NULL
+    assert epi(L, w=MIS) == binding.RET_ERR_ALIGN
+    assert epi(L, H=200) == binding.RET_ERR_UNSUPPORTED
+    assert epi(L, b=-2) == binding.RET_ERR_SHAPE
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    q = torch.zeros(1, 1, 16, 16)
+    with pytest.raises(ValueError):
+        binding.retention_parallel(q, q, q, [0.5])
