@@ -139,6 +139,23 @@ int retention_check_device_error(void* stream);
  */
 unsigned long long retention_kernel_launches(void);
 
+/* Kernel codes reported by retention_last_kernel(). */
+enum {
+    RET_KERNEL_NONE = 0,
+    RET_KERNEL_PARALLEL_SIMT = 1,   /* parallel form, CUDA-core fp32 FMA kernel       */
+    RET_KERNEL_CHUNKWISE_SIMT = 2,  /* chunkwise form, CUDA-core fp32 FMA kernel      */
+    RET_KERNEL_DECODE = 3,          /* recurrent step                                 */
+    RET_KERNEL_EPILOGUE = 4,        /* GroupNorm + swish gate                         */
+    RET_KERNEL_CHUNKWISE_TC = 5,    /* chunkwise form, tcgen05 tensor-core kernel     */
+    RET_KERNEL_PARALLEL_TC = 6      /* parallel form, tcgen05 tensor-core kernel      */
+};
+
+/*
+ * Code of the kernel the calling host thread launched last (RET_KERNEL_*),
+ * or RET_KERNEL_NONE if it has launched none.  Host-side, per thread.
+ */
+int retention_last_kernel(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,8 @@ RET_ERR_UNSUPPORTED, RET_ERR_CUDA, RET_ERR_TIMEOUT = 5, 6, 7
 RET_F32, RET_BF16 = 0, 1
 NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
+KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
+                5: "chunkwise_tc", 6: "parallel_tc"}
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +65,8 @@ def lib() -> ctypes.CDLL:
             L.retention_check_device_error.argtypes = [vp]
             L.retention_kernel_launches.argtypes = []
             L.retention_kernel_launches.restype = ctypes.c_ulonglong
+            L.retention_last_kernel.argtypes = []
+            L.retention_last_kernel.restype = ctypes.c_int
             for name in ("retention_parallel", "retention_chunkwise", "retention_recurrent_step",
                          "msr_epilogue", "retention_check_device_error"):
                 getattr(L, name).restype = ctypes.c_int
@@ -178,6 +182,11 @@ def msr_epilogue(y, g, eps: float = 1e-5, weight=None, bias=None, out=None,
 def kernel_launches() -> int:
     """Kernels the library has launched in this process (host-side counter)."""
     return int(lib().retention_kernel_launches())
+
+
+def last_kernel() -> str:
+    """Name of the kernel this host thread launched last (see RET_KERNEL_* codes)."""
+    return KERNEL_NAMES.get(int(lib().retention_last_kernel()), "unknown")
 
 
 def check_device_error(stream=None):

@@ -18,8 +18,10 @@ constexpr int kMaxHeads = 128;
 //   omg  = 1 - gamma
 //   gB   = gamma^B                (chunkwise only; gamma^1 elsewhere)
 //   g1   = gamma
+//   g128 = gamma^128
 struct HeadConsts {
     float g1[kMaxHeads];
+    float g128[kMaxHeads];
     float l2g[kMaxHeads];
     float lng[kMaxHeads];
     float omg[kMaxHeads];
@@ -86,8 +88,9 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
                                int out_bf16, int b, int H, int N, int dk, int dv,
                                const HeadConsts& hc, unsigned flags, cudaStream_t s);
-// Count one successful kernel launch (host-side, process-wide).
-void count_launch();
+// Count one successful kernel launch (host-side, process-wide) and record its
+// RET_KERNEL_* code for the launching host thread.
+void count_launch(int kernel_code);
 // Device error words of the kernels with bounded waits: read and clear.
 unsigned read_clear_error_tc_chunkwise(cudaStream_t s);
 unsigned read_clear_error_tc_parallel(cudaStream_t s);

@@ -100,7 +100,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, float* state, vo
         static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v), state,
         static_cast<TO*>(o), dk, dv, H, slices, hc);
     cudaError_t err = cudaGetLastError();
-    if (err == cudaSuccess) count_launch();
+    if (err == cudaSuccess) count_launch(RET_KERNEL_DECODE);
     return err;
 }
 

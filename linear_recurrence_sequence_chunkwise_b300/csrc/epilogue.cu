@@ -124,7 +124,7 @@ cudaError_t launch(const void* y, const void* g, void* out, int b, int H, int N,
         static_cast<const TY*>(y), static_cast<const TG*>(g), static_cast<TO*>(out), H, N, dv,
         groups, eps, w, bias);
     cudaError_t err = cudaGetLastError();
-    if (err == cudaSuccess) count_launch();
+    if (err == cudaSuccess) count_launch(RET_KERNEL_EPILOGUE);
     return err;
 }
 

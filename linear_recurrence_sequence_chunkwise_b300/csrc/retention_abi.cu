@@ -13,8 +13,12 @@ using ret::HeadConsts;
 namespace ret {
 namespace {
 std::atomic<unsigned long long> g_launches{0};
+thread_local int t_last_kernel = RET_KERNEL_NONE;
 }
-void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void count_launch(int kernel_code) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    t_last_kernel = kernel_code;
+}
 }  // namespace ret
 
 namespace {
@@ -37,6 +41,7 @@ int head_consts(const double* gamma, int H, int B, HeadConsts* hc) {
         hc->lng[h] = (g == 0.0) ? -INFINITY : (float)log(g);
         hc->omg[h] = (float)(1.0 - g);
         hc->g1[h] = (float)g;
+        hc->g128[h] = (float)pow(g, 128.0);
         hc->gB[h] = (float)pow(g, (double)B);
     }
     return RET_OK;
@@ -164,6 +169,8 @@ int msr_epilogue(const void* y, const void* g, void* out, ret_dtype y_dtype, ret
 }
 
 unsigned long long retention_kernel_launches(void) { return ret::g_launches.load(); }
+
+int retention_last_kernel(void) { return ret::t_last_kernel; }
 
 int retention_check_device_error(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -262,7 +262,7 @@ cudaError_t launch_par(const void* q, const void* k, const void* v, void* o, int
                                                static_cast<const TI*>(v), static_cast<TO*>(o), H, N,
                                                dk, dv, qtiles, flags, hc);
     cudaError_t err = cudaGetLastError();
-    if (err == cudaSuccess) count_launch();
+    if (err == cudaSuccess) count_launch(RET_KERNEL_PARALLEL_SIMT);
     return err;
 }
 
@@ -284,7 +284,7 @@ cudaError_t launch_chk(const void* q, const void* k, const void* v, void* o, int
                                                static_cast<const TI*>(v), static_cast<TO*>(o), H, N,
                                                dk, dv, B, slices, hc, si, so);
     cudaError_t err = cudaGetLastError();
-    if (err == cudaSuccess) count_launch();
+    if (err == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_SIMT);
     return err;
 }
 

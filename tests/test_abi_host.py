@@ -32,7 +32,8 @@ def test_exports_every_declared_function(L):
     names = binding.header_functions()
     assert set(names) == {"retention_parallel", "retention_chunkwise", "retention_recurrent_step",
                           "msr_epilogue", "retention_status_string",
-                          "retention_check_device_error", "retention_kernel_launches"}
+                          "retention_check_device_error", "retention_kernel_launches",
+                          "retention_last_kernel"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,

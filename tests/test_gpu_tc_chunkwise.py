@@ -1,0 +1,106 @@
+"""Tensor-core (tcgen05) chunkwise kernel against the oracle.
+
+Shapes the tensor-core kernel takes: bf16 inputs, dk in {128, 256}, dv a
+multiple of 64, chunk in {128, 256}, every gamma >= 2^-0.5.  Each test also
+checks that this kernel, not the CUDA-core one, ran.
+"""
+import pytest
+import torch
+
+import oracle
+from linear_recurrence_sequence_chunkwise_b300 import binding as rb
+from linear_recurrence_sequence_chunkwise_b300 import inputs
+
+from _util import TOL_BF16, err_bf16, err_bf16_out, err_f32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    rb.lib()
+
+
+def mk(b, H, N, dk, dv, seed, std=1 / 16):
+    q = inputs.randn((b, H, N, dk), seed, std, "bf16", DEV)
+    k = inputs.randn((b, H, N, dk), seed + 1, std, "bf16", DEV)
+    v = inputs.randn((b, H, N, dv), seed + 2, std, "bf16", DEV)
+    return q, k, v
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+@pytest.mark.parametrize("dk,dv", [(256, 512), (128, 64), (256, 192), (128, 128)])
+def test_tc_chunkwise_shapes(chunk, dk, dv):
+    b, H, N = 2, 2, 1024
+    q, k, v = mk(b, H, N, dk, dv, 100 + dk + dv)
+    g = [0.96875, 0.9990234375]
+    got = rb.retention_chunkwise(q, k, v, g, chunk)
+    assert rb.last_kernel() == "chunkwise_tc"
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
+    rb.check_device_error()
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+def test_tc_chunkwise_decay_range(chunk):
+    """From the smallest decay the folded factors allow (0.75) to almost 1."""
+    b, H, N, dk, dv = 1, 4, 768, 128, 64
+    q, k, v = mk(b, H, N, dk, dv, 200)
+    g = [0.75, 0.9, 0.999, 1.0 - 2.0 ** -20]
+    got = rb.retention_chunkwise(q, k, v, g, chunk)
+    assert rb.last_kernel() == "chunkwise_tc"
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
+
+
+def test_tc_chunkwise_unit_scale_inputs():
+    """N(0,1) inputs (outputs far from unit scale) still match to 2e-2 of RMS."""
+    b, H, N, dk, dv = 1, 2, 512, 256, 128
+    q, k, v = mk(b, H, N, dk, dv, 300, std=1.0)
+    g = inputs.gammas(H)
+    got = rb.retention_chunkwise(q, k, v, g, 256)
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, 256)) < TOL_BF16
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+def test_tc_chunkwise_states_and_bf16_out(chunk):
+    """state_in/state_out (aliased) continue a sequence exactly like one long call."""
+    b, H, N, dk, dv = 2, 3, 1024, 256, 128
+    q, k, v = mk(b, H, N, dk, dv, 400)
+    g = [0.98, 0.995, 0.9999]
+    want, s_end = oracle.chunkwise(q, k, v, g, chunk, return_state=True)
+    st = torch.zeros(b, H, dk, dv, device=DEV)
+    half = N // 2
+    parts = []
+    for lo in (0, half):
+        sl = slice(lo, lo + half)
+        parts.append(rb.retention_chunkwise(q[:, :, sl].contiguous(), k[:, :, sl].contiguous(),
+                                            v[:, :, sl].contiguous(), g, chunk,
+                                            state_in=st if lo else None, state_out=st,
+                                            out_dtype=torch.bfloat16))
+        assert rb.last_kernel() == "chunkwise_tc"
+    assert err_bf16_out(torch.cat(parts, dim=2), want) < 1.0
+    assert err_f32(st, s_end) < TOL_BF16
+
+
+def test_tc_chunkwise_nonzero_state_in():
+    b, H, N, dk, dv = 1, 2, 512, 128, 128
+    q, k, v = mk(b, H, N, dk, dv, 500)
+    g = [0.97, 0.995]
+    s0 = inputs.randn((b, H, dk, dv), 501, 0.1, "f32", DEV)
+    so = torch.empty_like(s0)
+    got = rb.retention_chunkwise(q, k, v, g, 256, state_in=s0, state_out=so)
+    want, s_end = oracle.chunkwise(q, k, v, g, 256, state_in=s0, return_state=True)
+    assert err_bf16(got, want) < TOL_BF16
+    assert err_f32(so, s_end) < TOL_BF16
+
+
+def test_small_decay_uses_cuda_core_kernel():
+    """gamma < 2^-0.5 falls outside the folded-factor range: CUDA-core kernel."""
+    b, H, N, dk, dv = 1, 2, 256, 128, 64
+    q, k, v = mk(b, H, N, dk, dv, 600)
+    g = [0.5, 0.9]
+    got = rb.retention_chunkwise(q, k, v, g, 128)
+    assert rb.last_kernel() == "chunkwise_simt"
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, 128)) < TOL_BF16
