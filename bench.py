@@ -387,6 +387,51 @@ def run_ours(args, dist: Dist):
     return 0
 
 
+# ----------------------------------------------------------------------------- profiling
+PROFILE_CASES = {
+    # reduced sizes of the benched workloads, inputs still larger than L2
+    "chunkwise": "chunkwise_long at N=8192: b1 H16 dk256 dv512 chunk 256, bf16 in, fp32 out",
+    "decode": "decode at b32: H16 dk256 dv512, fp32 state (268 MB), bf16 q/k/v, fp32 out",
+    "parallel": "parallel_norm at b2: H8 N2048 dk256 dv512, all normalisations, + epilogue",
+}
+
+
+def run_profile(case: str) -> int:
+    """Two untimed calls of one workload at a reduced size (the first is a warm-up
+    that an ncu capture skips with -s).  For ncu captures only; prints no timing."""
+    from linear_recurrence_sequence_chunkwise_b300 import binding as rb
+    rb.lib()
+    if case == "chunkwise":
+        w = inputs.CHUNKWISE_LONG
+        q, k, v = inputs.qkv(w, "cuda", N=8192)
+        o = torch.empty(w.b, w.H, 8192, w.dv, dtype=torch.float32, device="cuda")
+        calls = [lambda: rb.retention_chunkwise(q, k, v, w.gamma, w.chunk, out=o)]
+    elif case == "decode":
+        w = inputs.DECODE
+        state = inputs.randn((32, w.H, w.dk, w.dv), w.seed + 5, w.state_std, "f32", "cuda")
+        qs, ks, vs = (inputs.randn((32, w.H, d), w.seed + 101 + i, w.scale, "bf16", "cuda")
+                      for i, d in enumerate((w.dk, w.dk, w.dv)))
+        o = torch.empty(32, w.H, w.dv, dtype=torch.float32, device="cuda")
+        calls = [lambda: rb.retention_recurrent_step(qs, ks, vs, state, w.gamma, out=o)]
+    else:
+        w = inputs.PARALLEL_NORM
+        q, k, v = inputs.qkv(inputs.Workload("p", 2, w.H, w.N, w.dk, w.dv, w.dtype, w.scale,
+                                             flags=w.flags, seed=w.seed))
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        g = inputs.randn((2, w.N, w.H * w.dv), w.seed + 4, 1.0, "bf16", "cuda")
+        y = torch.empty(2, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+        out = torch.empty(2, w.N, w.H * w.dv, dtype=torch.float32, device="cuda")
+        calls = [lambda: rb.retention_parallel(q, k, v, w.gamma, w.flags, out=y),
+                 lambda: rb.msr_epilogue(y, g, w.eps, out=out)]
+    for _ in range(2):
+        for c in calls:
+            c()
+    rb.check_device_error()
+    torch.cuda.synchronize()
+    print(f"profile case {case}: {PROFILE_CASES[case]}; launches {rb.kernel_launches()}")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -396,7 +441,11 @@ def main(argv=None):
     ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--only-headline", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES), default=None,
+                    help="run two untimed calls of one reduced workload (for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile(args.profile)
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     dist = Dist()
     if args.impl == "reference":
