@@ -19,6 +19,7 @@ constexpr int kMaxHeads = 128;
 //   gB   = gamma^B                (chunkwise only; gamma^1 elsewhere)
 //   g1   = gamma
 //   g128 = gamma^128
+//   ginvB = gamma^(-B)          (chunkwise only; +inf for gamma = 0)
 struct HeadConsts {
     float g1[kMaxHeads];
     float g128[kMaxHeads];
@@ -26,6 +27,7 @@ struct HeadConsts {
     float lng[kMaxHeads];
     float omg[kMaxHeads];
     float gB[kMaxHeads];
+    float ginvB[kMaxHeads];
 };
 
 // gamma^e for an integer exponent e >= 0 from log2(gamma): exp2(e * log2 gamma),

@@ -43,6 +43,7 @@ int head_consts(const double* gamma, int H, int B, HeadConsts* hc) {
         hc->g1[h] = (float)g;
         hc->g128[h] = (float)pow(g, 128.0);
         hc->gB[h] = (float)pow(g, (double)B);
+        hc->ginvB[h] = (g == 0.0) ? INFINITY : (float)pow(g, -(double)B);
     }
     return RET_OK;
 }

@@ -1,7 +1,8 @@
 """Tensor-core (tcgen05) chunkwise kernel against the oracle.
 
 Shapes the tensor-core kernel takes: bf16 inputs, dk in {128, 256}, dv a
-multiple of 64, chunk in {128, 256}, every gamma >= 2^-0.5.  Each test also
+multiple of 64, chunk in {128, 256}, every gamma with gamma^(-chunk) <= 2^64
+(gamma >= 2^-0.5 at chunk 128, >= 2^-0.25 at chunk 256).  Each test also
 checks that this kernel, not the CUDA-core one, ran.
 """
 import pytest
@@ -45,10 +46,10 @@ def test_tc_chunkwise_shapes(chunk, dk, dv):
 
 @pytest.mark.parametrize("chunk", [128, 256])
 def test_tc_chunkwise_decay_range(chunk):
-    """From the smallest decay the folded factors allow (0.75) to almost 1."""
+    """From the smallest decay the folded factors allow to almost 1."""
     b, H, N, dk, dv = 1, 4, 768, 128, 64
     q, k, v = mk(b, H, N, dk, dv, 200)
-    g = [0.75, 0.9, 0.999, 1.0 - 2.0 ** -20]
+    g = [0.71 if chunk == 128 else 0.845, 0.9, 0.999, 1.0 - 2.0 ** -20]
     got = rb.retention_chunkwise(q, k, v, g, chunk)
     assert rb.last_kernel() == "chunkwise_tc"
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
@@ -96,11 +97,30 @@ def test_tc_chunkwise_nonzero_state_in():
     assert err_f32(so, s_end) < TOL_BF16
 
 
-def test_small_decay_uses_cuda_core_kernel():
-    """gamma < 2^-0.5 falls outside the folded-factor range: CUDA-core kernel."""
-    b, H, N, dk, dv = 1, 2, 256, 128, 64
+@pytest.mark.parametrize("chunk,gmin", [(128, 0.70), (256, 0.84)])
+def test_small_decay_uses_cuda_core_kernel(chunk, gmin):
+    """gamma^(-chunk) above 2^64 falls outside the folded-factor range: CUDA-core kernel."""
+    b, H, N, dk, dv = 1, 2, 512, 128, 64
     q, k, v = mk(b, H, N, dk, dv, 600)
-    g = [0.5, 0.9]
-    got = rb.retention_chunkwise(q, k, v, g, 128)
+    g = [gmin, 0.9]
+    got = rb.retention_chunkwise(q, k, v, g, chunk)
     assert rb.last_kernel() == "chunkwise_simt"
-    assert err_bf16(got, oracle.chunkwise(q, k, v, g, 128)) < TOL_BF16
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+def test_tc_chunkwise_repeatable_and_guarded(chunk):
+    """Two calls give bit-identical results; guard bands around O stay intact."""
+    from _util import guarded, guards_intact
+    b, H, N, dk, dv = 1, 3, 512, 256, 192
+    q, k, v = mk(b, H, N, dk, dv, 700)
+    g = inputs.gammas(H)
+    buf, o = guarded((b, H, N, dv), torch.float32, DEV)
+    rb.retention_chunkwise(q, k, v, g, chunk, out=o)
+    first = o.clone()
+    rb.retention_chunkwise(q, k, v, g, chunk, out=o)
+    torch.cuda.synchronize()
+    assert rb.last_kernel() == "chunkwise_tc"
+    assert torch.equal(first, o)
+    assert guards_intact(buf)
+    assert err_bf16(o, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
