@@ -139,6 +139,16 @@ int retention_check_device_error(void* stream);
  */
 unsigned long long retention_kernel_launches(void);
 
+/*
+ * cudaError_t value of the most recent CUDA failure (launch, attribute or
+ * runtime call) that made a call of this host thread return RET_ERR_CUDA,
+ * 0 if none.  Host-side, per thread; never cleared by successful calls.
+ */
+int retention_last_cuda_error(void);
+
+/* Static name and description of a cudaError_t value, e.g. "cudaErrorLaunchOutOfResources: ...". */
+const char* retention_cuda_error_string(int cuda_error);
+
 /* Kernel codes reported by retention_last_kernel(). */
 enum {
     RET_KERNEL_NONE = 0,

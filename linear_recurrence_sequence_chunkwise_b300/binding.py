@@ -67,6 +67,10 @@ def lib() -> ctypes.CDLL:
             L.retention_kernel_launches.restype = ctypes.c_ulonglong
             L.retention_last_kernel.argtypes = []
             L.retention_last_kernel.restype = ctypes.c_int
+            L.retention_last_cuda_error.argtypes = []
+            L.retention_last_cuda_error.restype = ctypes.c_int
+            L.retention_cuda_error_string.argtypes = [ctypes.c_int]
+            L.retention_cuda_error_string.restype = ctypes.c_char_p
             for name in ("retention_parallel", "retention_chunkwise", "retention_recurrent_step",
                          "msr_epilogue", "retention_check_device_error"):
                 getattr(L, name).restype = ctypes.c_int
@@ -80,7 +84,11 @@ def status_string(status: int) -> str:
 
 def _check(func: str, rc: int):
     if rc != RET_OK:
-        raise RetentionError(func, rc, status_string(rc))
+        text = status_string(rc)
+        if rc == RET_ERR_CUDA:
+            ce = int(lib().retention_last_cuda_error())
+            text += "; " + lib().retention_cuda_error_string(ce).decode()
+        raise RetentionError(func, rc, text)
 
 
 def _dtype_code(t: torch.dtype) -> int:

@@ -2,6 +2,7 @@
 // constants, kernel selection.  Host code only; kernels live in the other files.
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -14,6 +15,7 @@ namespace ret {
 namespace {
 std::atomic<unsigned long long> g_launches{0};
 thread_local int t_last_kernel = RET_KERNEL_NONE;
+thread_local int t_last_cuda_error = 0;
 }
 void count_launch(int kernel_code) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -48,7 +50,11 @@ int head_consts(const double* gamma, int H, int B, HeadConsts* hc) {
     return RET_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? RET_OK : RET_ERR_CUDA; }
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return RET_OK;
+    ret::t_last_cuda_error = (int)e;
+    return RET_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -173,11 +179,22 @@ unsigned long long retention_kernel_launches(void) { return ret::g_launches.load
 
 int retention_last_kernel(void) { return ret::t_last_kernel; }
 
+int retention_last_cuda_error(void) { return ret::t_last_cuda_error; }
+
+const char* retention_cuda_error_string(int cuda_error) {
+    static thread_local char buf[256];
+    const cudaError_t e = static_cast<cudaError_t>(cuda_error);
+    snprintf(buf, sizeof(buf), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return buf;
+}
+
 int retention_check_device_error(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return RET_ERR_CUDA;
+    cudaError_t ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) return cuda_status(ce);
     unsigned e = ret::read_clear_error_tc_chunkwise(s) | ret::read_clear_error_tc_parallel(s);
-    if (cudaGetLastError() != cudaSuccess) return RET_ERR_CUDA;
+    ce = cudaGetLastError();
+    if (ce != cudaSuccess) return cuda_status(ce);
     return e ? RET_ERR_TIMEOUT : RET_OK;
 }
 

@@ -41,9 +41,9 @@
 //   [  0,128) R: state, dk rows 0-127 (cols 0-63) and 128-255 (cols 64-127)
 //   [128,256) O: two 64-column accumulators (row blocks of a 256-chunk, or
 //             alternating chunks when B = 128)
-//   [256,512) S: two 128-column score buffers.  P is written in place as bf16 pairs:
-//             keys 0-63 -> hi at +0..31, lo at +32..63; keys 64-127 -> hi at
-//             +64..95, lo at +96..127; the P.V MMAs read it as their A operand.
+//   [256,512) S: two 128-column score buffers.  P is written in place as bf16 pairs,
+//             per 32 keys (32 columns of S): hi pairs in the first 16 columns, lo
+//             pairs in the next 16; the P.V MMAs read it as their A operand.
 // Shared memory (1024-aligned, 224 KB): 4 ring stages x 32 KB (one piece = 128 rows
 //   x 128 columns of Q or K, two 64-column 128B-swizzled atoms), 2 x 16 KB scaled V
 //   blocks, 2 x 32 KB bf16 hi/lo copies of R_{i-1} (B operand of q R).
@@ -117,7 +117,7 @@ __device__ __forceinline__ uint32_t piece_index(int which_k, int rb, int hh, int
     return (uint32_t)((2 * rb + which_k) * nh + hh);
 }
 
-template <bool OUT_BF16>
+template <int NH, int NRB, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, void* __restrict__ out,
@@ -137,7 +137,8 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     const int nblk = dv / 64;
     const int bh = blockIdx.x / nblk, blk = blockIdx.x % nblk;
     const int head = bh % H;
-    const int nrb = B / 128, nh = dk / 128, nchunks = N / B;
+    constexpr int nrb = NRB, nh = NH;
+    const int nchunks = N / B;
     const uint32_t per_chunk = (uint32_t)(2 * nrb * nh);   // ring pieces per chunk
     volatile int* abort_p = &abort_flag;
 
@@ -231,13 +232,16 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                 if (ok && !mbar_wait(bar, par, abort_p)) { ok = false; fail(abort_p); }
                 return ok;
             };
-            auto piece_addr = [&](uint32_t f) { return ring_a + (f % kStages) * kStage; };
+            // Descriptors are linear in the start-address field (address >> 4, low 14 bits),
+            // so every operand descriptor is a base descriptor plus a byte offset / 16.
+            const uint64_t dK = sdesc_sw128(ring_a, 16, 1024);      // K-major, ring base
+            const uint64_t dMN = sdesc_sw128(ring_a, kAtom, 1024);  // MN-major, ring base
+            const uint64_t dVz = sdesc_sw128(vz_a, kAtom, 1024);
+            const uint64_t dRhi = sdesc_sw128(rhi_a, kAtom, 1024);
+            const uint64_t dRlo = sdesc_sw128(rlo_a, kAtom, 1024);
+            auto slot_off = [&](uint32_t f) { return (uint64_t)(((f % kStages) * kStage) >> 4); };
             auto wait_piece = [&](uint32_t f) { return wait(&bars.full[f % kStages], (f / kStages) & 1); };
             auto release_piece = [&](uint32_t f) { mma_commit(&bars.empty[f % kStages]); };
-            auto kmaj = [&](uint32_t base, int which, int rb, int k0) {
-                const uint32_t off = ((k0 % 128) / 64) * kAtom + (k0 % 64) * 2;
-                return sdesc_sw128(piece_addr(base + piece_index(which, rb, k0 / 128, nh)) + off, 16, 1024);
-            };
             // S(sb) = Q_rb K_cb^T  (M=128, N=128, K=dk), waiting for each dk half's pieces
             // just before its k-steps; the buffer must have been read by its previous P.V.
             auto mma_s = [&](uint32_t base, int rb, int cb, int sb) {
@@ -249,8 +253,13 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                     wait_piece(base + piece_index(1, cb, hh, nh));
                     if (!ok) return;
                     tc_fence_after();
-                    for (int k0 = 128 * hh; k0 < 128 * hh + 128; k0 += 16)
-                        mma_bf16(ts, kmaj(base, 0, rb, k0), kmaj(base, 1, cb, k0), id_s, k0 > 0);
+                    const uint64_t da = dK + slot_off(base + piece_index(0, rb, hh, nh));
+                    const uint64_t db = dK + slot_off(base + piece_index(1, cb, hh, nh));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t off = (uint64_t)((((kk * 16) / 64) * kAtom + ((kk * 16) % 64) * 2) >> 4);
+                        mma_bf16(ts, da + off, db + off, id_s, (hh | kk) != 0);
+                    }
                 }
                 mma_commit(&bars.s_full[sb]);
                 ++su;
@@ -262,10 +271,16 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                 if (!ok) return;
                 tc_fence_after();
                 const uint32_t to = tmem + kTO + 64 * ob;
-                for (int k0 = 0; k0 < dk; k0 += 16) {
-                    const uint64_t ad = kmaj(base, 0, rb, k0);
-                    mma_bf16(to, ad, sdesc_sw128(rhi_a + k0 * 128, kAtom, 1024), id_q, k0 > 0);
-                    mma_bf16(to, ad, sdesc_sw128(rlo_a + k0 * 128, kAtom, 1024), id_q, 1);
+#pragma unroll 1
+                for (int hh = 0; hh < nh; ++hh) {
+                    const uint64_t da = dK + slot_off(base + piece_index(0, rb, hh, nh));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = da + (uint64_t)((((kk * 16) / 64) * kAtom + ((kk * 16) % 64) * 2) >> 4);
+                        const uint64_t rof = (uint64_t)(hh * ((128 * 128) >> 4) + ((16 * kk * 128) >> 4));
+                        mma_bf16(to, ad, dRhi + rof, id_q, (hh | kk) != 0);
+                        mma_bf16(to, ad, dRlo + rof, id_q, 1);
+                    }
                 }
                 ++ou;
             };
@@ -275,11 +290,13 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                 if (!wait(&bars.p_ready[sb], pu & 1)) return;
                 tc_fence_after();
                 const uint32_t ts = tmem + kTS + 128 * sb;
+                const uint64_t dv0 = dVz + (uint64_t)((vb * kAtom) >> 4);
+#pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    const uint32_t a_hi = ts + (t < 4 ? 8 * t : 64 + 8 * (t - 4));
-                    const uint64_t bd = sdesc_sw128(vz_a + vb * kAtom + 16 * t * 128, kAtom, 1024);
+                    const uint32_t a_hi = ts + 32 * (t / 2) + 8 * (t % 2);
+                    const uint64_t bd = dv0 + (uint64_t)((16 * t * 128) >> 4);
                     mma_ts(tmem + kTO + 64 * ob, a_hi, bd, id_p, 1);
-                    mma_ts(tmem + kTO + 64 * ob, a_hi + 32, bd, id_p, 1);
+                    mma_ts(tmem + kTO + 64 * ob, a_hi + 16, bd, id_p, 1);
                 }
                 mma_commit(&bars.pv_done[sb]);
                 ++pu;
@@ -288,13 +305,15 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
             // piece as soon as its half is issued when `release` is set.
             auto mma_kv = [&](uint32_t base, int cb, int vb, bool release) {
                 tc_fence_after();
+                const uint64_t dv0 = dVz + (uint64_t)((vb * kAtom) >> 4);
+#pragma unroll 1
                 for (int hh = 0; hh < nh; ++hh) {
                     const uint32_t f = base + piece_index(1, cb, hh, nh);
-                    const uint32_t ka = piece_addr(f);
-                    for (int t0 = 0; t0 < 128; t0 += 16) {
-                        const uint64_t ad = sdesc_sw128(ka + t0 * 128, kAtom, 1024);
-                        const uint64_t bd = sdesc_sw128(vz_a + vb * kAtom + t0 * 128, kAtom, 1024);
-                        mma_bf16(tmem + kTR + 64 * hh, ad, bd, id_r, 1);
+                    const uint64_t da = dMN + slot_off(f);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const uint64_t off = (uint64_t)((16 * t * 128) >> 4);
+                        mma_bf16(tmem + kTR + 64 * hh, da + off, dv0 + off, id_r, 1);
                     }
                     if (release) release_piece(f);
                 }
@@ -381,27 +400,25 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                 ++sc;
                 tc_fence_after();
                 const uint32_t ts = tmem + lrow + kTS + 128 * sb;
+                // quarter qq of the keys (32 columns of S) becomes 16 hi and 16 lo columns
+                // in the same 32 columns: read all of it before writing any of it
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float x[64];
-                    tmem_ld32(ts + 64 * half, x);
-                    tmem_ld32(ts + 64 * half + 32, x + 32);
+                for (int qq = 0; qq < 4; ++qq) {
+                    float x[32];
+                    tmem_ld32(ts + 32 * qq, x);
                     tmem_wait_ld();
-                    uint32_t ph[32], pl[32];
+                    uint32_t pp[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int kc = 64 * half + 2 * e;
+                    for (int e = 0; e < 16; ++e) {
+                        const int kc = 32 * qq + 2 * e;
                         float x0 = x[2 * e] * cP, x1 = x[2 * e + 1] * cP;
                         if (diag) {
                             if (kc > row) x0 = 0.f;
                             if (kc + 1 > row) x1 = 0.f;
                         }
-                        split2(x0, x1, ph[e], pl[e]);
+                        split2(x0, x1, pp[e], pp[16 + e]);
                     }
-                    tmem_st16(ts + 64 * half, ph);
-                    tmem_st16(ts + 64 * half + 16, ph + 16);
-                    tmem_st16(ts + 64 * half + 32, pl);
-                    tmem_st16(ts + 64 * half + 48, pl + 16);
+                    tmem_st32(ts + 32 * qq, reinterpret_cast<const float*>(pp));
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -588,7 +605,19 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
     const long long grid = (long long)b * H * (dv / 64);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = kSmemBytes + 1024;
-    auto kern = out_bf16 ? chunkwise_tc_kernel<true> : chunkwise_tc_kernel<false>;
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, void*, const float*,
+                 float*, int, int, int, int, int, const Decay);
+    const int sel = (dk == 256 ? 4 : 0) + (chunk == 256 ? 2 : 0) + (out_bf16 ? 1 : 0);
+    switch (sel) {
+        case 0: kern = chunkwise_tc_kernel<1, 1, false>; break;
+        case 1: kern = chunkwise_tc_kernel<1, 1, true>; break;
+        case 2: kern = chunkwise_tc_kernel<1, 2, false>; break;
+        case 3: kern = chunkwise_tc_kernel<1, 2, true>; break;
+        case 4: kern = chunkwise_tc_kernel<2, 1, false>; break;
+        case 5: kern = chunkwise_tc_kernel<2, 1, true>; break;
+        case 6: kern = chunkwise_tc_kernel<2, 2, false>; break;
+        default: kern = chunkwise_tc_kernel<2, 2, true>; break;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, chunk, H,

@@ -33,7 +33,8 @@ def test_exports_every_declared_function(L):
     assert set(names) == {"retention_parallel", "retention_chunkwise", "retention_recurrent_step",
                           "msr_epilogue", "retention_status_string",
                           "retention_check_device_error", "retention_kernel_launches",
-                          "retention_last_kernel"}
+                          "retention_last_kernel", "retention_last_cuda_error",
+                          "retention_cuda_error_string"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
@@ -46,6 +47,12 @@ def test_launch_counter_starts_at_zero_and_rejections_do_not_count(L):
     before = binding.kernel_launches()
     assert par(L, dk=24) == binding.RET_ERR_UNSUPPORTED
     assert binding.kernel_launches() == before
+
+
+def test_cuda_error_query(L):
+    assert L.retention_last_cuda_error() == 0          # nothing has failed on this thread
+    assert binding.lib().retention_cuda_error_string(0).startswith(b"cudaSuccess")
+    assert b"cudaErrorLaunchOutOfResources" in binding.lib().retention_cuda_error_string(701)
 
 
 def test_status_strings(L):
