@@ -1,0 +1,97 @@
+"""Tensor-core (tcgen05) parallel-form kernel against the oracle.
+
+Shapes the tensor-core kernel takes: bf16 inputs, dk in {128, 256}, dv a multiple
+of 128, any N >= 128 (a partial last query/key tile is masked), any gamma in [0, 1], all
+normalisation flags.  Each test also checks that this kernel, not the CUDA-core
+one, ran.  Tolerance: bf16 inputs with fp32 accumulation, 2e-2 of the output RMS
+(bf16 outputs add their own rounding), as in tests/_util.py.
+"""
+import pytest
+import torch
+
+import oracle
+from linear_recurrence_sequence_chunkwise_b300 import binding as rb
+from linear_recurrence_sequence_chunkwise_b300 import inputs
+
+from _util import TOL_BF16, err_bf16, err_bf16_out, guarded, guards_intact
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    rb.lib()
+
+
+def mk(b, H, N, dk, dv, seed, std=1.0):
+    q = inputs.randn((b, H, N, dk), seed, std, "bf16", DEV)
+    k = inputs.randn((b, H, N, dk), seed + 1, std, "bf16", DEV)
+    v = inputs.randn((b, H, N, dv), seed + 2, std, "bf16", DEV)
+    return q, k, v
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 4, 7])
+@pytest.mark.parametrize("dk,dv", [(256, 512), (128, 128), (256, 384), (128, 256)])
+def test_tc_parallel_shapes_and_flags(dk, dv, flags):
+    b, H, N = 1, 2, 384
+    q, k, v = mk(b, H, N, dk, dv, 1000 + dk + dv + flags)
+    g = [0.96875, 0.9990234375]
+    got = rb.retention_parallel(q, k, v, g, flags)
+    assert rb.last_kernel() == "parallel_tc"
+    assert err_bf16(got, oracle.parallel(q, k, v, g, flags)) < TOL_BF16
+    rb.check_device_error()
+
+
+@pytest.mark.parametrize("N", [1, 77, 128, 129, 200, 520])
+def test_tc_parallel_ragged_sequence(N):
+    """N not a multiple of the 128-row tile: the partial tiles are masked (N < 128
+    goes to the CUDA-core kernel)."""
+    b, H, dk, dv = 2, 2, 256, 256
+    q, k, v = mk(b, H, N, dk, dv, 2000 + N)
+    g = [0.9, 0.99]
+    got = rb.retention_parallel(q, k, v, g, 7)
+    assert rb.last_kernel() == ("parallel_tc" if N >= 128 else "parallel_simt")
+    assert err_bf16(got, oracle.parallel(q, k, v, g, 7)) < TOL_BF16
+
+
+def test_tc_parallel_special_decays():
+    """gamma = 0 (diagonal only) and gamma = 1 (causal linear attention)."""
+    b, H, N, dk, dv = 1, 2, 300, 128, 128
+    q, k, v = mk(b, H, N, dk, dv, 3000, std=0.25)
+    g = [0.0, 1.0]
+    for flags in (0, 2, 7):
+        got = rb.retention_parallel(q, k, v, g, flags)
+        assert rb.last_kernel() == "parallel_tc"
+        assert err_bf16(got, oracle.parallel(q, k, v, g, flags)) < TOL_BF16, flags
+
+
+def test_tc_parallel_bf16_output_guarded_and_repeatable():
+    b, H, N, dk, dv = 2, 3, 260, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 4000)
+    g = inputs.gammas(H)
+    buf, o = guarded((b, H, N, dv), torch.bfloat16, DEV)
+    rb.retention_parallel(q, k, v, g, 7, out=o)
+    first = o.clone()
+    rb.retention_parallel(q, k, v, g, 7, out=o)
+    torch.cuda.synchronize()
+    assert rb.last_kernel() == "parallel_tc"
+    assert torch.equal(first, o)
+    assert guards_intact(buf)
+    assert err_bf16_out(o, oracle.parallel(q, k, v, g, 7)) < 1.0
+
+
+def test_tc_parallel_matches_cuda_core_kernel_on_fp32_copy():
+    """The same inputs held in fp32 take the CUDA-core kernel; both agree with the oracle."""
+    b, H, N, dk, dv = 1, 2, 256, 128, 128
+    q, k, v = mk(b, H, N, dk, dv, 5000)
+    g = [0.95, 0.999]
+    a = rb.retention_parallel(q, k, v, g, 7)
+    assert rb.last_kernel() == "parallel_tc"
+    c = rb.retention_parallel(q.float(), k.float(), v.float(), g, 7)
+    assert rb.last_kernel() == "parallel_simt"
+    want = oracle.parallel(q, k, v, g, 7)
+    assert err_bf16(a, want) < TOL_BF16
+    assert err_bf16(c, want) < 1e-4
