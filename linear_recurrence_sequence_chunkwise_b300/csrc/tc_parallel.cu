@@ -70,7 +70,7 @@ struct ParConsts {
 struct Bars {
     uint64_t q_full;
     uint64_t full[kRing], empty[kRing];
-    uint64_t s_full[2], p_ready[2], pv_done[2];
+    uint64_t s_full[2], p_ready[2];
     uint64_t o_full;
     uint64_t drain;
 };
@@ -99,6 +99,7 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float rs_part[2][128];
+    __shared__ __align__(16) float colf[128];     // g^(-j), j = key column in a tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (N + 127) / 128;
@@ -117,7 +118,6 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         for (int s = 0; s < kRing; ++s) { mbar_init(&bars.full[s], 1); mbar_init(&bars.empty[s], 1); }
         for (int c = 0; c < 2; ++c) {
             mbar_init(&bars.s_full[c], 1); mbar_init(&bars.p_ready[c], kXWarps);
-            mbar_init(&bars.pv_done[c], 1);
         }
         mbar_init(&bars.o_full, 1);
         mbar_init(&bars.drain, 1);
@@ -183,7 +183,9 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             for (int st = 0; st <= T && ok; ++st) {
                 if (st < T) {
                     const int sb = st & 1;
-                    if (st >= 2) wait(&bars.pv_done[sb], ((st - 2) >> 1) & 1);
+                    // S(st) overwrites the buffer P(st-2) was read from: tcgen05.mma
+                    // operations of one thread execute in issue order, so P(st-2).V,
+                    // issued earlier, has read it first.
                     for (int hh = 0; hh < NH; ++hh) wait(&bars.full[(fill + hh) % kRing], ((fill + hh) / kRing) & 1);
                     if (!ok) break;
                     tc_fence_after();
@@ -220,7 +222,6 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                             mma_ts(tmem + kTO + 128 * vp, a_t + 16, bd, id_p, 1);
                         }
                     }
-                    mma_commit(&bars.pv_done[sb]);
                     for (int vp = 0; vp < NV; ++vp) mma_commit(&bars.empty[(fill + vp) % kRing]);
                     fill += NV;
                 }
@@ -240,6 +241,12 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         float rowc = (flags & RET_NORM_SCALE) ? rsqrtf((float)dk) : 1.0f;
         if (flags & RET_NORM_DECAY) rowc *= rsqrtf(decay_rowsum(pc.lng[head], pc.omg[head], n));
         const bool want_rs = (flags & RET_NORM_ROWSUM) != 0;
+        // g^(n-m) = g^(n-m0) * g^(-(m-m0)): one exp2 per row and tile, times a column
+        // factor from a table.  The factors stay in range while g^(-127) <= 2^64; a
+        // smaller g takes one exp2 per element.
+        const bool factored = l2g >= -0.5f;
+        if (grp == 0) colf[row] = factored ? exp2f(-l2g * (float)row) : 0.f;
+        named_bar(1, kXWarps * 32);
         float rs = 0.f;
         bool ok = true;
         auto wait = [&](uint64_t* bar, uint32_t par) {
@@ -254,18 +261,28 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc_fence_after();
             const uint32_t ts = tmem + lrow + kTS + 128 * sb;
             const int m0 = 128 * t;
+            const float a = rowc * (factored ? decay_pow(l2g, (float)(n - m0)) : 1.0f);
 #pragma unroll 1
             for (int c32 = 0; c32 < 2; ++c32) {
                 const int kc = 64 * grp + 32 * c32;
                 float x[32];
                 tmem_ld32(ts + kc, x);
+                float cf[32];
+                const float4* cp = reinterpret_cast<const float4*>(colf + kc);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 f = cp[j];
+                    cf[4 * j] = f.x; cf[4 * j + 1] = f.y; cf[4 * j + 2] = f.z; cf[4 * j + 3] = f.w;
+                }
                 tmem_wait_ld();
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int m = m0 + kc + 2 * e;
-                    const float p0 = (m <= n) ? x[2 * e] * rowc * decay_pow(l2g, (float)(n - m)) : 0.f;
-                    const float p1 = (m + 1 <= n) ? x[2 * e + 1] * rowc * decay_pow(l2g, (float)(n - m - 1)) : 0.f;
+                    const float w0 = factored ? a * cf[2 * e] : rowc * decay_pow(l2g, (float)(n - m));
+                    const float w1 = factored ? a * cf[2 * e + 1] : rowc * decay_pow(l2g, (float)(n - m - 1));
+                    const float p0 = (m <= n) ? x[2 * e] * w0 : 0.f;
+                    const float p1 = (m + 1 <= n) ? x[2 * e + 1] * w1 : 0.f;
                     if (want_rs) rs += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                     pk[16 + e] = pack_bf16(p0 - __uint_as_float(pk[e] << 16),
@@ -281,7 +298,7 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         }
         // ---- output: O / max(|row sum|, 1) for rows inside the sequence
         rs_part[grp][row] = rs;
-        named_bar(1, kXWarps * 32);
+        named_bar(2, kXWarps * 32);
         float den = 1.f;
         if (want_rs) den = fmaxf(fabsf(rs_part[0][row] + rs_part[1][row]), 1.0f);
         const float inv = 1.0f / den;
