@@ -392,7 +392,7 @@ PROFILE_CASES = {
     # reduced sizes of the benched workloads, inputs still larger than L2
     "chunkwise": "chunkwise_long at N=8192: b1 H16 dk256 dv512 chunk 256, bf16 in, fp32 out",
     "decode": "decode at b32: H16 dk256 dv512, fp32 state (268 MB), bf16 q/k/v, fp32 out",
-    "parallel": "parallel_norm at b2: H8 N2048 dk256 dv512, all normalisations, + epilogue",
+    "parallel": "parallel_norm (b8 H8 N2048 dk256 dv512, all normalisations) + epilogue",
 }
 
 
@@ -415,12 +415,10 @@ def run_profile(case: str) -> int:
         calls = [lambda: rb.retention_recurrent_step(qs, ks, vs, state, w.gamma, out=o)]
     else:
         w = inputs.PARALLEL_NORM
-        q, k, v = inputs.qkv(inputs.Workload("p", 2, w.H, w.N, w.dk, w.dv, w.dtype, w.scale,
-                                             flags=w.flags, seed=w.seed))
-        q, k, v = q.cuda(), k.cuda(), v.cuda()
-        g = inputs.randn((2, w.N, w.H * w.dv), w.seed + 4, 1.0, "bf16", "cuda")
-        y = torch.empty(2, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
-        out = torch.empty(2, w.N, w.H * w.dv, dtype=torch.float32, device="cuda")
+        q, k, v = inputs.qkv(w, "cuda")
+        g = inputs.gate(w, "cuda")
+        y = torch.empty(w.b, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+        out = torch.empty(w.b, w.N, w.H * w.dv, dtype=torch.float32, device="cuda")
         calls = [lambda: rb.retention_parallel(q, k, v, w.gamma, w.flags, out=y),
                  lambda: rb.msr_epilogue(y, g, w.eps, out=out)]
     for _ in range(2):
