@@ -326,12 +326,11 @@ def bench_parallel(args, dist, rb, pk):
     w = inputs.PARALLEL_NORM
     q, k, v = inputs.qkv(w, "cuda")
     g = inputs.gate(w, "cuda")
-    y = torch.empty(w.b, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
     out = torch.empty(w.b, w.N, w.H * w.dv, dtype=torch.float32, device="cuda")
 
     def step():
-        rb.retention_parallel(q, k, v, w.gamma, w.flags, out=y)
-        rb.msr_epilogue(y, g, w.eps, out=out)
+        # one kernel: parallel form, normalisations, GroupNorm and swish gate
+        rb.retention_parallel_gated(q, k, v, g, w.gamma, w.flags, w.eps, out=out)
 
     steps = max(3, args.steps // 2)
     ms, _ = timed(step, steps, max(1, args.warmup // 2), dist)
@@ -341,10 +340,11 @@ def bench_parallel(args, dist, rb, pk):
     value, _ = aggregate(dist, ms, tokens * steps)
     flops = inputs.algorithmic_flops("parallel", w)
     achieved = flops / (ms_step * 1e-3) / 1e12
-    del q, k, v, g, y, out
+    del q, k, v, g, out
     torch.cuda.empty_cache()
     return {"workload": f"{w.name}: b{w.b} H{w.H} N{w.N} dk{w.dk} dv{w.dv}, bf16 in, all three "
-                        "normalisations, GroupNorm(eps 1e-5)+swish gate epilogue, fp32 out",
+                        "normalisations, GroupNorm(eps 1e-5)+swish gate epilogue fused "
+                        "(retention_parallel_gated), fp32 out",
             "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
@@ -417,10 +417,8 @@ def run_profile(case: str) -> int:
         w = inputs.PARALLEL_NORM
         q, k, v = inputs.qkv(w, "cuda")
         g = inputs.gate(w, "cuda")
-        y = torch.empty(w.b, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
         out = torch.empty(w.b, w.N, w.H * w.dv, dtype=torch.float32, device="cuda")
-        calls = [lambda: rb.retention_parallel(q, k, v, w.gamma, w.flags, out=y),
-                 lambda: rb.msr_epilogue(y, g, w.eps, out=out)]
+        calls = [lambda: rb.retention_parallel_gated(q, k, v, g, w.gamma, w.flags, w.eps, out=out)]
     for _ in range(2):
         for c in calls:
             c()

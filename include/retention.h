@@ -121,6 +121,26 @@ int msr_epilogue(const void* y, const void* g, void* out, ret_dtype y_dtype,
                  ret_dtype g_dtype, ret_dtype out_dtype, int b, int H, int N, int dv,
                  float eps, const float* weight, const float* bias, void* stream);
 
+/*
+ * Parallel form and gated epilogue in one pass ([RN2] "Retention" 1) eq.(5) with the
+ * factors of "Retention Score 歸一化", then "門控多尺度 Retention"); the retention output
+ * Y is never written to memory:
+ *   Y[b][h][n][:] = retention_parallel(q, k, v, gamma, flags) for that (b, h, n)
+ *   out[b][n][h*dv + c] = swish(g[b][n][h*dv + c]) * GN(Y[b][h][n][:])[c]
+ *   GN(y)[c] = (y[c] - mean(y)) / sqrt(var(y) + eps) [* weight[h*dv+c] + bias[h*dv+c]]
+ * (biased variance over the dv values of one (token, head)).
+ * q, k: [b][H][N][dk], v: [b][H][N][dv] in in_dtype; g, out: [b][N][H*dv] (token-major)
+ * in g_dtype / out_dtype; weight, bias: H*dv floats on the DEVICE, each nullable.
+ * Tensor-core shapes only: in_dtype RET_BF16, dk in {128, 256}, dv a multiple of 128 and
+ * at most 512, N >= 128.  Other shapes return RET_ERR_UNSUPPORTED before any launch;
+ * retention_parallel followed by msr_epilogue computes the same result for them.
+ */
+int retention_parallel_gated(const void* q, const void* k, const void* v, const void* g,
+                             void* out, ret_dtype in_dtype, ret_dtype g_dtype,
+                             ret_dtype out_dtype, int b, int H, int N, int dk, int dv,
+                             const double* gamma, unsigned flags, float eps,
+                             const float* weight, const float* bias, void* stream);
+
 /* Static text for a ret_status code ("unknown status" for other values). */
 const char* retention_status_string(int status);
 
@@ -157,7 +177,8 @@ enum {
     RET_KERNEL_DECODE = 3,          /* recurrent step                                 */
     RET_KERNEL_EPILOGUE = 4,        /* GroupNorm + swish gate                         */
     RET_KERNEL_CHUNKWISE_TC = 5,    /* chunkwise form, tcgen05 tensor-core kernel     */
-    RET_KERNEL_PARALLEL_TC = 6      /* parallel form, tcgen05 tensor-core kernel      */
+    RET_KERNEL_PARALLEL_TC = 6,     /* parallel form, tcgen05 tensor-core kernel      */
+    RET_KERNEL_PARALLEL_GATED_TC = 7 /* parallel form + gated GroupNorm, tensor cores */
 };
 
 /*

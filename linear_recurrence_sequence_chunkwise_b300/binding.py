@@ -24,7 +24,7 @@ RET_F32, RET_BF16 = 0, 1
 NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
-                5: "chunkwise_tc", 6: "parallel_tc"}
+                5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc"}
 
 _lib = None
 _lock = threading.Lock()
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.retention_chunkwise.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp, vp, vp, vp]
             L.retention_recurrent_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, dp, vp]
             L.msr_epilogue.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, vp]
+            L.retention_parallel_gated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp,
+                                                   u, f, vp, vp, vp]
             L.retention_status_string.argtypes = [i]
             L.retention_status_string.restype = ctypes.c_char_p
             L.retention_check_device_error.argtypes = [vp]
@@ -72,7 +74,8 @@ def lib() -> ctypes.CDLL:
             L.retention_cuda_error_string.argtypes = [ctypes.c_int]
             L.retention_cuda_error_string.restype = ctypes.c_char_p
             for name in ("retention_parallel", "retention_chunkwise", "retention_recurrent_step",
-                         "msr_epilogue", "retention_check_device_error"):
+                         "msr_epilogue", "retention_check_device_error",
+                         "retention_parallel_gated"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -184,6 +187,25 @@ def msr_epilogue(y, g, eps: float = 1e-5, weight=None, bias=None, out=None,
                             _dtype_code(g.dtype), _dtype_code(out.dtype), b, H, N, dv,
                             float(eps), _ptr(weight), _ptr(bias), _stream(stream))
     _check("msr_epilogue", rc)
+    return out
+
+
+def retention_parallel_gated(q, k, v, g, gamma, flags: int = 0, eps: float = 1e-5, weight=None,
+                             bias=None, out=None, out_dtype=torch.float32, stream=None):
+    """Parallel form + GroupNorm/swish-gate epilogue in one kernel.  q,k:[b,H,N,dk]
+    v:[b,H,N,dv] (bf16), g:[b,N,H*dv]; returns out [b,N,H*dv]."""
+    b, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((b, N, H * dv), dtype=out_dtype, device=q.device)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    rc = lib().retention_parallel_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out),
+                                        _dtype_code(q.dtype), _dtype_code(g.dtype),
+                                        _dtype_code(out.dtype), b, H, N, dk, dv, _gamma(gamma, H),
+                                        flags, float(eps), _ptr(weight), _ptr(bias),
+                                        _stream(stream))
+    _check("retention_parallel_gated", rc)
     return out
 
 

@@ -90,6 +90,11 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
                                int out_bf16, int b, int H, int N, int dk, int dv,
                                const HeadConsts& hc, unsigned flags, cudaStream_t s);
+cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v, const void* g,
+                                     void* out, int g_bf16, int out_bf16, int b, int H, int N,
+                                     int dk, int dv, const HeadConsts& hc, unsigned flags,
+                                     float eps, const float* weight, const float* bias,
+                                     cudaStream_t s);
 // Count one successful kernel launch (host-side, process-wide) and record its
 // RET_KERNEL_* code for the launching host thread.
 void count_launch(int kernel_code);

@@ -97,6 +97,35 @@ int retention_parallel(const void* q, const void* k, const void* v, void* o,
                                                  dk, dv, hc, flags, s));
 }
 
+int retention_parallel_gated(const void* q, const void* k, const void* v, const void* g,
+                             void* out, ret_dtype in_dtype, ret_dtype g_dtype,
+                             ret_dtype out_dtype, int b, int H, int N, int dk, int dv,
+                             const double* gamma, unsigned flags, float eps,
+                             const float* weight, const float* bias, void* stream) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(g_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (flags & ~(RET_NORM_SCALE | RET_NORM_DECAY | RET_NORM_ROWSUM)) return RET_ERR_UNSUPPORTED;
+    if (!dims_ok(dk, dv)) return RET_ERR_UNSUPPORTED;
+    if (!(eps >= 0.0f) || isinf(eps)) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || H == 0 || N == 0) return RET_OK;
+    if (!q || !k || !v || !g || !out || !gamma) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out))
+        return RET_ERR_ALIGN;
+    if ((weight && !aligned16(weight)) || (bias && !aligned16(bias))) return RET_ERR_ALIGN;
+    // tensor-core shapes only (see the header)
+    if (in_dtype != RET_BF16 || !(dk == 128 || dk == 256) || dv % 128 != 0 || N < 128)
+        return RET_ERR_UNSUPPORTED;
+    HeadConsts hc;
+    int rc = head_consts(gamma, H, 1, &hc);
+    if (rc != RET_OK) return rc;
+    cudaError_t e = ret::launch_parallel_gated_tc(q, k, v, g, out, g_dtype == RET_BF16,
+                                                  out_dtype == RET_BF16, b, H, N, dk, dv, hc,
+                                                  flags, eps, weight, bias,
+                                                  static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return RET_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
 int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
                         ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N, int dk,
                         int dv, int chunk, const double* gamma, const float* state_in,

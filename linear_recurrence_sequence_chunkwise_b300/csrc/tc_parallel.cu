@@ -10,8 +10,8 @@
 // Work split: one CTA per (batch*head, 128-row query tile, block of W = 256 (or
 // 128) value columns).  The score tile S = Q_rb K_cb^T does not depend on the
 // value columns; the dv/W CTAs of a query tile each compute it (dk/(dk+W) of their
-// tensor work).  Heavy query tiles (more key tiles under the causal mask) are
-// scheduled first.
+// tensor work).  Within each group of 8 heads, heavy query tiles (more key tiles under
+// the causal mask) are scheduled first.
 //
 // Per key tile cb (128 keys):
 //   S(cb) = Q K_cb^T                      tcgen05 M=128 N=128, K=dk, into a TMEM buffer
@@ -67,6 +67,17 @@ struct ParConsts {
     float omg[kMaxHeads];
 };
 
+// Fused gated epilogue ([RN2] "門控多尺度 Retention"): GroupNorm over the dv outputs of
+// each (token, head), optional per-channel affine, times swish(G).
+struct EpiArgs {
+    const void* g;          // [b][N][H*dv], fp32 or bf16 (template EPI)
+    const float* weight;    // [H*dv] or NULL
+    const float* bias;      // [H*dv] or NULL
+    float eps;
+};
+constexpr int kMaxClusterCtas = 4;   // value-column blocks of one query tile
+constexpr int kHeadGroup = 8;        // (batch, head) pairs whose CTAs are scheduled together
+
 struct Bars {
     uint64_t q_full;
     uint64_t full[kRing], empty[kRing];
@@ -85,11 +96,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-template <int NH, int NV, bool OUT_BF16>
+// EPI = 0: write O [b][H][N][dv].  EPI = 1 / 2: fused gated GroupNorm with G in fp32 /
+// bf16, writing [b][N][H*dv]; the nvb value-column blocks of a query tile then run as
+// one thread-block cluster and exchange per-row statistics through shared memory.
+template <int NH, int NV, bool OUT_BF16, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, void* __restrict__ out, int N, int H,
-                   int dk, int dv, int bH, int nvb, unsigned flags, const ParConsts pc) {
+                   int dk, int dv, int bH, int nvb, unsigned flags, const ParConsts pc,
+                   const EpiArgs ea) {
     constexpr int W = 128 * NV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -98,19 +113,32 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     __shared__ Bars bars;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    __shared__ float rs_part[2][128];
+    // Epilogue scratch, reusing the ring once every MMA of this CTA has completed (after
+    // o_full): row sums and statistics of the two transform groups, and (mean, M2) of
+    // each value-column block of the cluster, written by the peers.
+    float (*rs_part)[128] = reinterpret_cast<float (*)[128]>(ring);
+    float (*st_part)[128] = reinterpret_cast<float (*)[128]>(ring + 1024);
+    float2 (*peer_stats)[128] = reinterpret_cast<float2 (*)[128]>(ring + 2048);
     __shared__ __align__(16) float colf[128];     // g^(-j), j = key column in a tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Block order: groups of kHeadGroup (batch, head) pairs, inside a group heavy query
+    // tiles first, then (batch, head), then value-column block (the cluster).  The CTAs
+    // resident at one time then share the K/V of a few heads in L2 instead of streaming
+    // every head's K/V from DRAM.
     const int nqt = (N + 127) / 128;
-    const int per_qt = bH * nvb;
-    const int qt = nqt - 1 - (int)(blockIdx.x / per_qt);     // heavy query tiles first
-    const int rest = (int)(blockIdx.x % per_qt);
-    const int bh = rest / nvb, vb = rest % nvb;
+    const int full_grp = kHeadGroup * nqt * nvb;
+    const int gi = (int)(blockIdx.x / full_grp);
+    const int gheads = min(kHeadGroup, bH - gi * kHeadGroup);
+    const int r_in = (int)(blockIdx.x % full_grp);
+    const int qt = nqt - 1 - r_in / (gheads * nvb);
+    const int rest = r_in % (gheads * nvb);
+    const int bh = gi * kHeadGroup + rest / nvb, vb = rest % nvb;
     const int head = bh % H;
     const int n0 = 128 * qt;
     const int T = qt + 1;                                     // key tiles under the mask
     volatile int* abort_p = &abort_flag;
+    float stat_mean = 0.f, stat_m2 = 0.f, row_inv = 1.f;      // fused epilogue, per row
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -297,36 +325,170 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (lane == 0) mbar_arrive(&bars.p_ready[sb]);
         }
         // ---- output: O / max(|row sum|, 1) for rows inside the sequence
+        constexpr int kCols = W / 2;                            // value columns of this group
+        const uint32_t ocol = tmem + lrow + kTO + kCols * grp;
+        // warp-uniform: tcgen05.ld is warp-collective.  After o_full no MMA reads the ring.
+        const bool have_o = ok && wait(&bars.o_full, 0);
+        if (have_o) tc_fence_after();
         rs_part[grp][row] = rs;
         named_bar(2, kXWarps * 32);
         float den = 1.f;
         if (want_rs) den = fmaxf(fabsf(rs_part[0][row] + rs_part[1][row]), 1.0f);
         const float inv = 1.0f / den;
-        if (ok && wait(&bars.o_full, 0)) {
-            tc_fence_after();
-            constexpr int kCols = W / 2;                        // value columns of this group
-            const size_t orow = (size_t)bh * N + (size_t)n;
-            const size_t col0 = (size_t)W * vb + (size_t)kCols * grp;
+        if (EPI == 0) {
+            if (have_o) {
+                const size_t orow = (size_t)bh * N + (size_t)n;
+                const size_t col0 = (size_t)W * vb + (size_t)kCols * grp;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kCols; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem + lrow + kTO + kCols * grp + c0, o);
-                tmem_wait_ld();
-                if (n < N) {
-                    if (OUT_BF16) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + orow * dv + col0 + c0);
+                for (int c0 = 0; c0 < kCols; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(ocol + c0, o);
+                    tmem_wait_ld();
+                    if (n < N) {
+                        if (OUT_BF16) {
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + orow * dv + col0 + c0);
 #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            dst[cc] = make_uint4(pack_bf16(o[8 * cc] * inv, o[8 * cc + 1] * inv),
-                                                 pack_bf16(o[8 * cc + 2] * inv, o[8 * cc + 3] * inv),
-                                                 pack_bf16(o[8 * cc + 4] * inv, o[8 * cc + 5] * inv),
-                                                 pack_bf16(o[8 * cc + 6] * inv, o[8 * cc + 7] * inv));
+                            for (int cc = 0; cc < 4; ++cc)
+                                dst[cc] = make_uint4(pack_bf16(o[8 * cc] * inv, o[8 * cc + 1] * inv),
+                                                     pack_bf16(o[8 * cc + 2] * inv, o[8 * cc + 3] * inv),
+                                                     pack_bf16(o[8 * cc + 4] * inv, o[8 * cc + 5] * inv),
+                                                     pack_bf16(o[8 * cc + 6] * inv, o[8 * cc + 7] * inv));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + orow * dv + col0 + c0);
+#pragma unroll
+                            for (int cc = 0; cc < 8; ++cc)
+                                dst[cc] = make_float4(o[4 * cc] * inv, o[4 * cc + 1] * inv,
+                                                      o[4 * cc + 2] * inv, o[4 * cc + 3] * inv);
+                        }
+                    }
+                }
+            }
+        } else {
+            // statistics of this block's W values of the row: mean, then sum of squared
+            // deviations (two passes over tensor memory), combined over the two groups.
+            // Every transform warp takes part in the named barriers, aborted or not.
+            float s1 = 0.f;
+            if (have_o) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < kCols; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(ocol + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) s1 += o[j] * inv;
+                }
+            }
+            st_part[grp][row] = s1;
+            named_bar(3, kXWarps * 32);
+            const float mean_b = (st_part[0][row] + st_part[1][row]) / (float)W;
+            named_bar(4, kXWarps * 32);
+            float s2 = 0.f;
+            if (have_o) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < kCols; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(ocol + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) { const float d = o[j] * inv - mean_b; s2 += d * d; }
+                }
+            }
+            st_part[grp][row] = s2;
+            named_bar(5, kXWarps * 32);
+            if (grp == 0) {
+                stat_mean = mean_b;
+                stat_m2 = st_part[0][row] + st_part[1][row];
+            }
+            row_inv = inv;
+        }
+    }
+    if (EPI != 0) {
+        // 1st cluster barrier: every CTA of the query tile is past its last MMA, so its
+        // ring may receive the peers' statistics; 2nd: all statistics have arrived.
+        __syncwarp();
+        cluster_sync_all();
+        if (warp >= 2 && warp < 6) {
+            const int row = 32 * (warp & 3) + (threadIdx.x & 31);
+            for (int r = 0; r < nvb; ++r)
+                st_cluster_f32x2(map_peer(&peer_stats[vb][row], (uint32_t)r), stat_mean, stat_m2);
+        }
+        __syncwarp();
+        cluster_sync_all();
+        if (warp >= 2) {
+            const int grp = (warp - 2) >> 2;
+            const int q4 = warp & 3;
+            const int row = 32 * q4 + (threadIdx.x & 31);
+            const uint32_t lrow = (uint32_t)(32 * q4) << 16;
+            const int n = n0 + row;
+            const float inv = row_inv;
+            constexpr int kCols = W / 2;
+            float mean = 0.f;
+            for (int r = 0; r < nvb; ++r) mean += peer_stats[r][row].x;
+            mean /= (float)nvb;
+            float m2 = 0.f;
+            for (int r = 0; r < nvb; ++r) {
+                const float d = peer_stats[r][row].x - mean;
+                m2 += peer_stats[r][row].y + (float)W * d * d;
+            }
+            const float rstd = rsqrtf(m2 / (float)dv + ea.eps);
+            const int bi = bh / H;
+            const size_t grow = ((size_t)bi * N + (size_t)n) * (size_t)H * dv;   // token-major row
+            const int ch0 = head * dv + W * vb + kCols * grp;                      // first channel
+            const bool live = __all_sync(0xffffffffu, abort_flag == 0);
+            if (live) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < kCols; c0 += 32) {
+                    float o[32], gv[32];
+                    tmem_ld32(tmem + lrow + kTO + kCols * grp + c0, o);
+                    if (n >= N) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) gv[j] = 0.f;
+                    } else if (EPI == 2) {
+                        const uint4* gp = reinterpret_cast<const uint4*>(
+                            static_cast<const __nv_bfloat16*>(ea.g) + grow + ch0 + c0);
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const uint4 u = gp[cc];
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                gv[8 * cc + 2 * e] = __uint_as_float(w4[e] << 16);
+                                gv[8 * cc + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                            }
+                        }
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + orow * dv + col0 + c0);
+                        const float4* gp = reinterpret_cast<const float4*>(
+                            static_cast<const float*>(ea.g) + grow + ch0 + c0);
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc)
-                            dst[cc] = make_float4(o[4 * cc] * inv, o[4 * cc + 1] * inv,
-                                                  o[4 * cc + 2] * inv, o[4 * cc + 3] * inv);
+                        for (int cc = 0; cc < 8; ++cc) {
+                            const float4 f = gp[cc];
+                            gv[4 * cc] = f.x; gv[4 * cc + 1] = f.y; gv[4 * cc + 2] = f.z; gv[4 * cc + 3] = f.w;
+                        }
+                    }
+                    tmem_wait_ld();
+                    float r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float yn = (o[j] * inv - mean) * rstd;
+                        const int ch = ch0 + c0 + j;
+                        if (ea.weight) yn *= ea.weight[ch];
+                        if (ea.bias) yn += ea.bias[ch];
+                        r[j] = gv[j] / (1.0f + expf(-gv[j])) * yn;
+                    }
+                    if (n < N) {
+                        if (OUT_BF16) {
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + grow + ch0 + c0);
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc)
+                                dst[cc] = make_uint4(pack_bf16(r[8 * cc], r[8 * cc + 1]), pack_bf16(r[8 * cc + 2], r[8 * cc + 3]),
+                                                     pack_bf16(r[8 * cc + 4], r[8 * cc + 5]), pack_bf16(r[8 * cc + 6], r[8 * cc + 7]));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + grow + ch0 + c0);
+#pragma unroll
+                            for (int cc = 0; cc < 8; ++cc)
+                                dst[cc] = make_float4(r[4 * cc], r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3]);
+                        }
                     }
                 }
             }
@@ -343,13 +505,36 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
 }  // namespace
 
-cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o, int out_bf16,
-                               int b, int H, int N, int dk, int dv, const HeadConsts& hc,
-                               unsigned flags, cudaStream_t s) {
+namespace {
+
+using ParKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, void*, int, int,
+                           int, int, int, int, unsigned, const ParConsts, const EpiArgs);
+
+template <int EPI>
+ParKernel pick(int nh, int nv, int out_bf16) {
+    const int sel = (nh == 2 ? 4 : 0) + (nv == 2 ? 2 : 0) + (out_bf16 ? 1 : 0);
+    switch (sel) {
+        case 0: return parallel_tc_kernel<1, 1, false, EPI>;
+        case 1: return parallel_tc_kernel<1, 1, true, EPI>;
+        case 2: return parallel_tc_kernel<1, 2, false, EPI>;
+        case 3: return parallel_tc_kernel<1, 2, true, EPI>;
+        case 4: return parallel_tc_kernel<2, 1, false, EPI>;
+        case 5: return parallel_tc_kernel<2, 1, true, EPI>;
+        case 6: return parallel_tc_kernel<2, 2, false, EPI>;
+        default: return parallel_tc_kernel<2, 2, true, EPI>;
+    }
+}
+
+// epi: 0 plain output, 1 gated with fp32 G, 2 gated with bf16 G
+cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, int out_bf16, int b,
+                          int H, int N, int dk, int dv, const HeadConsts& hc, unsigned flags,
+                          int epi, const EpiArgs& ea, cudaStream_t s) {
     // the 128-row TMA boxes must fit the sequence; shorter ones go to the CUDA-core kernel
     if (!(dk == 128 || dk == 256) || dv % 128 != 0 || N < 128) return cudaErrorNotSupported;
     const int nv = (dv % 256 == 0) ? 2 : 1;
     const int W = 128 * nv;
+    const int nvb = dv / W;
+    if (epi != 0 && nvb > kMaxClusterCtas) return cudaErrorNotSupported;
     ParConsts pc;
     for (int h = 0; h < H; ++h) {
         pc.l2g[h] = hc.l2g[h];
@@ -362,29 +547,53 @@ cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void
     if (!make_map_bf16_3d(&mq, q, bH, N, dk, 128) || !make_map_bf16_3d(&mk, k, bH, N, dk, 128) ||
         !make_map_bf16_3d(&mv, v, bH, N, dv, 128))
         return cudaErrorInvalidValue;
-    const int nvb = dv / W;
     const long long grid = (long long)((N + 127) / 128) * bH * nvb;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = (dk / 128) * kPiece + kRing * kPiece + 1024;
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, void*, int, int, int, int,
-                 int, int, unsigned, const ParConsts);
-    const int sel = (dk == 256 ? 4 : 0) + (nv == 2 ? 2 : 0) + (out_bf16 ? 1 : 0);
-    switch (sel) {
-        case 0: kern = parallel_tc_kernel<1, 1, false>; break;
-        case 1: kern = parallel_tc_kernel<1, 1, true>; break;
-        case 2: kern = parallel_tc_kernel<1, 2, false>; break;
-        case 3: kern = parallel_tc_kernel<1, 2, true>; break;
-        case 4: kern = parallel_tc_kernel<2, 1, false>; break;
-        case 5: kern = parallel_tc_kernel<2, 1, true>; break;
-        case 6: kern = parallel_tc_kernel<2, 2, false>; break;
-        default: kern = parallel_tc_kernel<2, 2, true>; break;
-    }
+    ParKernel kern = epi == 0 ? pick<0>(dk / 128, nv, out_bf16)
+                   : epi == 1 ? pick<1>(dk / 128, nv, out_bf16) : pick<2>(dk / 128, nv, out_bf16);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, N, H, dk, dv, (int)bH, nvb, flags, pc);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) count_launch(RET_KERNEL_PARALLEL_TC);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (epi != 0) {
+        // the value-column blocks of one query tile exchange GroupNorm statistics
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)nvb;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, o, N, H, dk, dv, (int)bH, nvb, flags, pc, ea);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch(epi == 0 ? RET_KERNEL_PARALLEL_TC : RET_KERNEL_PARALLEL_GATED_TC);
     return e;
+}
+
+}  // namespace
+
+cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o, int out_bf16,
+                               int b, int H, int N, int dk, int dv, const HeadConsts& hc,
+                               unsigned flags, cudaStream_t s) {
+    return launch_common(q, k, v, o, out_bf16, b, H, N, dk, dv, hc, flags, 0, EpiArgs{}, s);
+}
+
+cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v, const void* g,
+                                     void* out, int g_bf16, int out_bf16, int b, int H, int N,
+                                     int dk, int dv, const HeadConsts& hc, unsigned flags,
+                                     float eps, const float* weight, const float* bias,
+                                     cudaStream_t s) {
+    EpiArgs ea;
+    ea.g = g;
+    ea.weight = weight;
+    ea.bias = bias;
+    ea.eps = eps;
+    return launch_common(q, k, v, out, out_bf16, b, H, N, dk, dv, hc, flags, g_bf16 ? 2 : 1, ea, s);
 }
 
 unsigned read_clear_error_tc_parallel(cudaStream_t s) {

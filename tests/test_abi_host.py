@@ -34,7 +34,7 @@ def test_exports_every_declared_function(L):
                           "msr_epilogue", "retention_status_string",
                           "retention_check_device_error", "retention_kernel_launches",
                           "retention_last_kernel", "retention_last_cuda_error",
-                          "retention_cuda_error_string"}
+                          "retention_cuda_error_string", "retention_parallel_gated"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
@@ -145,6 +145,31 @@ def test_epilogue_rejections(L):
     assert epi(L, w=MIS) == binding.RET_ERR_ALIGN
     assert epi(L, H=200) == binding.RET_ERR_UNSUPPORTED
     assert epi(L, b=-2) == binding.RET_ERR_SHAPE
+
+
+def gated(L, q=A, k=A, v=A, g=A, o=A2, it=1, gt=1, ot=0, b=1, H=2, N=256, dk=256, dv=512,
+          gam=None, flags=7, eps=1e-5, w=None, bias=None):
+    gam = G(0.9, 0.5) if gam is None else gam
+    return L.retention_parallel_gated(q, k, v, g, o, it, gt, ot, b, H, N, dk, dv, gam, flags,
+                                      ctypes.c_float(eps), w, bias, S)
+
+
+def test_parallel_gated_rejections(L):
+    assert gated(L, b=-1) == binding.RET_ERR_SHAPE
+    assert gated(L, gt=4) == binding.RET_ERR_DTYPE
+    assert gated(L, flags=16) == binding.RET_ERR_UNSUPPORTED
+    assert gated(L, eps=-1.0) == binding.RET_ERR_UNSUPPORTED
+    assert gated(L, g=NUL) == binding.RET_ERR_NULL
+    assert gated(L, g=MIS) == binding.RET_ERR_ALIGN
+    assert gated(L, bias=MIS) == binding.RET_ERR_ALIGN
+    # shapes outside the tensor-core kernel: documented as unsupported, nothing launched
+    before = binding.kernel_launches()
+    assert gated(L, it=0) == binding.RET_ERR_UNSUPPORTED          # fp32 inputs
+    assert gated(L, dk=64) == binding.RET_ERR_UNSUPPORTED
+    assert gated(L, dv=192) == binding.RET_ERR_UNSUPPORTED
+    assert gated(L, N=100) == binding.RET_ERR_UNSUPPORTED
+    assert gated(L, N=0, q=NUL, k=NUL, v=NUL, g=NUL, o=NUL) == binding.RET_OK
+    assert binding.kernel_launches() == before
 
 
 def test_binding_refuses_cpu_tensors(L):

@@ -86,6 +86,24 @@ def test_parallel_norm_full_with_epilogue():
         assert err_bf16(got_o, want_o) < TOL_BF16, (bi, h)
 
 
+def test_parallel_norm_full_fused_gated():
+    """The one-pass parallel + gated epilogue call bench.py times, at full size."""
+    w = inputs.PARALLEL_NORM
+    q, k, v = inputs.qkv(w, DEV)
+    g = inputs.gate(w, DEV)
+    out = rb.retention_parallel_gated(q, k, v, g, w.gamma, w.flags, w.eps)
+    assert rb.last_kernel() == "parallel_gated_tc"
+    rb.check_device_error()
+    idx = [(0, 0), (7, 7), (5, 2)]
+    us = units_of(q, k, v, idx)
+    ys = oracle.map_units(lambda u: oracle.parallel(u[2], u[3], u[4], [w.gamma[u[1]]], w.flags),
+                          us, threads=len(us))
+    for (bi, h, *_), y in zip(us, ys):
+        gu = g[bi:bi + 1, :, h * w.dv:(h + 1) * w.dv].cpu()
+        want = oracle.msr_epilogue(y, gu, w.eps)
+        assert err_bf16(out[bi:bi + 1, :, h * w.dv:(h + 1) * w.dv], want) < TOL_BF16, (bi, h)
+
+
 def test_decode_full_512_steps():
     w = inputs.DECODE
     s0 = inputs.decode_state(w, DEV)

@@ -95,3 +95,60 @@ def test_tc_parallel_matches_cuda_core_kernel_on_fp32_copy():
     want = oracle.parallel(q, k, v, g, 7)
     assert err_bf16(a, want) < TOL_BF16
     assert err_bf16(c, want) < 1e-4
+
+
+# ---------------------------------------------------------------- fused gated epilogue
+@pytest.mark.parametrize("dk,dv,N", [(256, 512, 256), (128, 256, 200), (256, 384, 384),
+                                     (128, 128, 130)])
+@pytest.mark.parametrize("flags", [0, 7])
+def test_tc_parallel_gated_matches_oracle(dk, dv, N, flags):
+    """GroupNorm over each (token, head) spans the value-column blocks of a cluster."""
+    b, H = 2, 2
+    q, k, v = mk(b, H, N, dk, dv, 6000 + dk + dv + N + flags)
+    gate = inputs.randn((b, N, H * dv), 6100 + N, 1.0, "bf16", DEV)
+    g = [0.96875, 0.999]
+    got = rb.retention_parallel_gated(q, k, v, gate, g, flags, 1e-5)
+    assert rb.last_kernel() == "parallel_gated_tc"
+    want = oracle.msr_epilogue(oracle.parallel(q, k, v, g, flags), gate, 1e-5)
+    assert err_bf16(got, want) < TOL_BF16
+    rb.check_device_error()
+
+
+@pytest.mark.parametrize("g_dtype,out_dtype", [(torch.float32, torch.float32),
+                                               (torch.bfloat16, torch.bfloat16)])
+def test_tc_parallel_gated_affine_dtypes_guarded(g_dtype, out_dtype):
+    b, H, N, dk, dv = 1, 3, 260, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 6500)
+    gate = inputs.randn((b, N, H * dv), 6501, 1.0, "f32", DEV).to(g_dtype)
+    w = inputs.randn((H * dv,), 6502, 1.0, "f32", DEV)
+    bias = inputs.randn((H * dv,), 6503, 1.0, "f32", DEV)
+    g = inputs.gammas(H)
+    buf, out = guarded((b, N, H * dv), out_dtype, DEV)
+    rb.retention_parallel_gated(q, k, v, gate, g, 7, 1e-5, w, bias, out=out)
+    torch.cuda.synchronize()
+    assert rb.last_kernel() == "parallel_gated_tc"
+    assert guards_intact(buf)
+    want = oracle.msr_epilogue(oracle.parallel(q, k, v, g, 7), gate, 1e-5, w, bias)
+    if out_dtype == torch.bfloat16:
+        assert err_bf16_out(out, want) < 1.0
+    else:
+        assert err_bf16(out, want) < TOL_BF16
+
+
+def test_tc_parallel_gated_equals_two_call_path():
+    """One pass equals retention_parallel followed by msr_epilogue on the GPU."""
+    b, H, N, dk, dv = 2, 2, 384, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 6600)
+    gate = inputs.randn((b, N, H * dv), 6601, 1.0, "bf16", DEV)
+    g = [0.9, 0.995]
+    fused = rb.retention_parallel_gated(q, k, v, gate, g, 7, 1e-5)
+    two = rb.msr_epilogue(rb.retention_parallel(q, k, v, g, 7), gate, 1e-5)
+    assert err_bf16(fused, two.cpu().double().numpy()) < 5e-3
+
+
+def test_tc_parallel_gated_unsupported_shape_is_rejected():
+    q, k, v = mk(1, 1, 256, 64, 64, 6700)
+    gate = inputs.randn((1, 256, 64), 6701, 1.0, "bf16", DEV)
+    with pytest.raises(rb.RetentionError) as ei:
+        rb.retention_parallel_gated(q, k, v, gate, [0.9], 7)
+    assert ei.value.status == rb.RET_ERR_UNSUPPORTED
