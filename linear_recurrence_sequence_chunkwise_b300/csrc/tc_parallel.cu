@@ -70,7 +70,7 @@ struct ParConsts {
 // Fused gated epilogue ([RN2] "門控多尺度 Retention"): GroupNorm over the dv outputs of
 // each (token, head), optional per-channel affine, times swish(G).
 struct EpiArgs {
-    const void* g;          // [b][N][H*dv], fp32 or bf16 (template EPI)
+    const void* g;          // [b][N][H*dv], fp32 or bf16 (template EPI); read through a TMA map
     const float* weight;    // [H*dv] or NULL
     const float* bias;      // [H*dv] or NULL
     float eps;
@@ -83,6 +83,8 @@ struct Bars {
     uint64_t full[kRing], empty[kRing];
     uint64_t s_full[2], p_ready[2];
     uint64_t o_full;
+    uint64_t g_full[2];
+    uint64_t q_free, g_pre;
     uint64_t drain;
 };
 
@@ -102,10 +104,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int NH, int NV, bool OUT_BF16, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                   const __grid_constant__ CUtensorMap mv, void* __restrict__ out, int N, int H,
-                   int dk, int dv, int bH, int nvb, unsigned flags, const ParConsts pc,
-                   const EpiArgs ea) {
+                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                   const __grid_constant__ CUtensorMap mg, int N, int H, int dk, int dv, int bH,
+                   int nvb, unsigned flags, const ParConsts pc, const EpiArgs ea) {
     constexpr int W = 128 * NV;
+    constexpr int kEpiChunks = W / 128;                   // 64-column chunks per group
+    // bf16 gate tiles of both groups fit where Q was: load them while the last P.V runs
+    constexpr bool kGPrefetch = (EPI == 2) && (2 * kEpiChunks * 16384 <= NH * kPiece);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* qarea = sm;
@@ -148,6 +153,8 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             mbar_init(&bars.s_full[c], 1); mbar_init(&bars.p_ready[c], kXWarps);
         }
         mbar_init(&bars.o_full, 1);
+        mbar_init(&bars.g_full[0], 1); mbar_init(&bars.g_full[1], 1);
+        mbar_init(&bars.q_free, 1); mbar_init(&bars.g_pre, 1);
         mbar_init(&bars.drain, 1);
         fence_barrier_init();
     }
@@ -161,6 +168,8 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv);
+            tma_prefetch_desc(&mo);
+            if (EPI != 0) tma_prefetch_desc(&mg);
             mbar_arrive_expect_tx(&bars.q_full, NH * kPiece);
             for (int hh = 0; hh < NH; ++hh)
                 for (int a = 0; a < 2; ++a)
@@ -184,11 +193,28 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     for (int vp = 0; vp < NV && ok; ++vp)
                         ok = load_piece(&mv, W * vb + 128 * vp, 128 * (st - 1));
             }
+            if (kGPrefetch && ok) {
+                // the last score MMA has read Q: its area takes the gate tiles
+                if (!mbar_wait(&bars.q_free, 0, abort_p)) {
+                    ok = false;
+                } else {
+                    mbar_arrive_expect_tx(&bars.g_pre, 2 * kEpiChunks * 16384);
+                    for (int gg = 0; gg < 2; ++gg)
+                        for (int ch = 0; ch < kEpiChunks; ++ch)
+                            tma_load_3d(qarea + (gg * kEpiChunks + ch) * 16384, &mg,
+                                        head * dv + W * vb + (W / 2) * gg + 64 * ch, n0, bh / H,
+                                        &bars.g_pre);
+                }
+            }
             if (!ok) {
                 fail(abort_p);
                 for (uint32_t f = fill > kRing ? fill - kRing : 0; f < fill; ++f)
                     mbar_wait(&bars.full[f % kRing], (f / kRing) & 1, nullptr, 100000000ull);
                 mbar_wait(&bars.q_full, 0, nullptr, 100000000ull);
+            }
+            if (kGPrefetch && !ok) {
+                // a gate load may be in flight only if it was issued; wait for it briefly
+                mbar_wait(&bars.g_pre, 0, nullptr, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -214,12 +240,12 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     // S(st) overwrites the buffer P(st-2) was read from: tcgen05.mma
                     // operations of one thread execute in issue order, so P(st-2).V,
                     // issued earlier, has read it first.
-                    for (int hh = 0; hh < NH; ++hh) wait(&bars.full[(fill + hh) % kRing], ((fill + hh) / kRing) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
                     const uint32_t ts = tmem + kTS + 128 * sb;
 #pragma unroll 1
                     for (int hh = 0; hh < NH; ++hh) {
+                        // each dk half waits for its own piece and frees it right away
+                        if (!wait(&bars.full[(fill + hh) % kRing], ((fill + hh) / kRing) & 1)) break;
+                        tc_fence_after();
                         const uint64_t da = dQ + (uint64_t)((hh * kPiece) >> 4);
                         const uint64_t db = dK + slot_off(fill + hh);
 #pragma unroll
@@ -227,20 +253,22 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                             const uint64_t off = (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4);
                             mma_bf16(ts, da + off, db + off, id_s, (hh | kk) != 0);
                         }
+                        mma_commit(&bars.empty[(fill + hh) % kRing]);
                     }
+                    if (!ok) break;
                     mma_commit(&bars.s_full[sb]);
-                    for (int hh = 0; hh < NH; ++hh) mma_commit(&bars.empty[(fill + hh) % kRing]);
+                    if (kGPrefetch && st == T - 1) mma_commit(&bars.q_free);
                     fill += NH;
                 }
                 if (st >= 1) {
                     const int t = st - 1, sb = t & 1;
-                    wait(&bars.p_ready[sb], (t >> 1) & 1);
-                    for (int vp = 0; vp < NV; ++vp) wait(&bars.full[(fill + vp) % kRing], ((fill + vp) / kRing) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
+                    if (!wait(&bars.p_ready[sb], (t >> 1) & 1)) break;
                     const uint32_t ts = tmem + kTS + 128 * sb;
 #pragma unroll 1
                     for (int vp = 0; vp < NV; ++vp) {
+                        // each 128-column value piece waits for its own load, frees it after use
+                        if (!wait(&bars.full[(fill + vp) % kRing], ((fill + vp) / kRing) & 1)) break;
+                        tc_fence_after();
                         const uint64_t db = dV + slot_off(fill + vp);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
@@ -249,8 +277,9 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                             mma_ts(tmem + kTO + 128 * vp, a_t, bd, id_p, (t | kk) != 0);
                             mma_ts(tmem + kTO + 128 * vp, a_t + 16, bd, id_p, 1);
                         }
+                        mma_commit(&bars.empty[(fill + vp) % kRing]);
                     }
-                    for (int vp = 0; vp < NV; ++vp) mma_commit(&bars.empty[(fill + vp) % kRing]);
+                    if (!ok) break;
                     fill += NV;
                 }
             }
@@ -336,33 +365,7 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         if (want_rs) den = fmaxf(fabsf(rs_part[0][row] + rs_part[1][row]), 1.0f);
         const float inv = 1.0f / den;
         if (EPI == 0) {
-            if (have_o) {
-                const size_t orow = (size_t)bh * N + (size_t)n;
-                const size_t col0 = (size_t)W * vb + (size_t)kCols * grp;
-#pragma unroll 1
-                for (int c0 = 0; c0 < kCols; c0 += 32) {
-                    float o[32];
-                    tmem_ld32(ocol + c0, o);
-                    tmem_wait_ld();
-                    if (n < N) {
-                        if (OUT_BF16) {
-                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + orow * dv + col0 + c0);
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc)
-                                dst[cc] = make_uint4(pack_bf16(o[8 * cc] * inv, o[8 * cc + 1] * inv),
-                                                     pack_bf16(o[8 * cc + 2] * inv, o[8 * cc + 3] * inv),
-                                                     pack_bf16(o[8 * cc + 4] * inv, o[8 * cc + 5] * inv),
-                                                     pack_bf16(o[8 * cc + 6] * inv, o[8 * cc + 7] * inv));
-                        } else {
-                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + orow * dv + col0 + c0);
-#pragma unroll
-                            for (int cc = 0; cc < 8; ++cc)
-                                dst[cc] = make_float4(o[4 * cc] * inv, o[4 * cc + 1] * inv,
-                                                      o[4 * cc + 2] * inv, o[4 * cc + 3] * inv);
-                        }
-                    }
-                }
-            }
+            row_inv = inv;
         } else {
             // statistics of this block's W values of the row: mean, then sum of squared
             // deviations (two passes over tensor memory), combined over the two groups.
@@ -414,15 +417,27 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         }
         __syncwarp();
         cluster_sync_all();
-        if (warp >= 2) {
-            const int grp = (warp - 2) >> 2;
-            const int q4 = warp & 3;
-            const int row = 32 * q4 + (threadIdx.x & 31);
-            const uint32_t lrow = (uint32_t)(32 * q4) << 16;
-            const int n = n0 + row;
-            const float inv = row_inv;
-            constexpr int kCols = W / 2;
-            float mean = 0.f;
+    }
+    // ---- staged output: per transform group, 64-column chunks of the group's W/2 columns.
+    // The ring is free once o_full has completed; each group uses 64 KB of it: a gate
+    // tile (TMA load) and an output tile (written here, stored by TMA, rows past N are
+    // clipped by the store).  Both tiles use the 128-byte swizzle: the 16-byte chunk c of
+    // row r sits at chunk position c ^ (r % 8) of a 128-row x 128-byte atom.
+    if (warp >= 2) {
+        const int grp = (warp - 2) >> 2;
+        const int q4 = warp & 3;
+        const int lane = threadIdx.x & 31;
+        const int row = 32 * q4 + lane;
+        const uint32_t lrow = (uint32_t)(32 * q4) << 16;
+        const bool issuer = (threadIdx.x == (unsigned)(64 + 128 * grp));   // lane 0 of warp 2 / 6
+        constexpr int kCols = W / 2;
+        constexpr int kChunks = kEpiChunks;
+        constexpr int kOutAtoms = OUT_BF16 ? 1 : 2;
+        constexpr int kGAtoms = (EPI == 2) ? 1 : 2;
+        uint8_t* ost = ring + 8192 + grp * 65536 + 32768;  // output staging (up to 2 atoms)
+        const float inv = row_inv;
+        float mean = 0.f, rstd = 1.f;
+        if (EPI != 0) {
             for (int r = 0; r < nvb; ++r) mean += peer_stats[r][row].x;
             mean /= (float)nvb;
             float m2 = 0.f;
@@ -430,69 +445,95 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const float d = peer_stats[r][row].x - mean;
                 m2 += peer_stats[r][row].y + (float)W * d * d;
             }
-            const float rstd = rsqrtf(m2 / (float)dv + ea.eps);
-            const int bi = bh / H;
-            const size_t grow = ((size_t)bi * N + (size_t)n) * (size_t)H * dv;   // token-major row
-            const int ch0 = head * dv + W * vb + kCols * grp;                      // first channel
-            const bool live = __all_sync(0xffffffffu, abort_flag == 0);
-            if (live) {
-                tc_fence_after();
+            rstd = rsqrtf(m2 / (float)dv + ea.eps);
+        }
+        const int bi = bh / H;
+        const bool live = __all_sync(0xffffffffu, abort_flag == 0);
+        if (live) tc_fence_after();
+        auto swz = [&](int c16) { return (uint32_t)(row * 128 + ((((uint32_t)c16) ^ (row & 7)) << 4)); };
 #pragma unroll 1
-                for (int c0 = 0; c0 < kCols; c0 += 32) {
-                    float o[32], gv[32];
-                    tmem_ld32(tmem + lrow + kTO + kCols * grp + c0, o);
-                    if (n >= N) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) gv[j] = 0.f;
-                    } else if (EPI == 2) {
-                        const uint4* gp = reinterpret_cast<const uint4*>(
-                            static_cast<const __nv_bfloat16*>(ea.g) + grow + ch0 + c0);
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const uint4 u = gp[cc];
-                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                gv[8 * cc + 2 * e] = __uint_as_float(w4[e] << 16);
-                                gv[8 * cc + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-                            }
-                        }
-                    } else {
-                        const float4* gp = reinterpret_cast<const float4*>(
-                            static_cast<const float*>(ea.g) + grow + ch0 + c0);
-#pragma unroll
-                        for (int cc = 0; cc < 8; ++cc) {
-                            const float4 f = gp[cc];
-                            gv[4 * cc] = f.x; gv[4 * cc + 1] = f.y; gv[4 * cc + 2] = f.z; gv[4 * cc + 3] = f.w;
-                        }
-                    }
-                    tmem_wait_ld();
-                    float r[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        float yn = (o[j] * inv - mean) * rstd;
-                        const int ch = ch0 + c0 + j;
-                        if (ea.weight) yn *= ea.weight[ch];
-                        if (ea.bias) yn += ea.bias[ch];
-                        r[j] = gv[j] / (1.0f + expf(-gv[j])) * yn;
-                    }
-                    if (n < N) {
-                        if (OUT_BF16) {
-                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + grow + ch0 + c0);
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc)
-                                dst[cc] = make_uint4(pack_bf16(r[8 * cc], r[8 * cc + 1]), pack_bf16(r[8 * cc + 2], r[8 * cc + 3]),
-                                                     pack_bf16(r[8 * cc + 4], r[8 * cc + 5]), pack_bf16(r[8 * cc + 6], r[8 * cc + 7]));
-                        } else {
-                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + grow + ch0 + c0);
-#pragma unroll
-                            for (int cc = 0; cc < 8; ++cc)
-                                dst[cc] = make_float4(r[4 * cc], r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3]);
-                        }
-                    }
+        for (int ch = 0; ch < kChunks; ++ch) {
+            const int col = W * vb + kCols * grp + 64 * ch;          // first value column
+            const int gcol = (EPI != 0) ? head * dv + col : col;     // column in the global map
+            const int plane = (EPI != 0) ? bi : bh;
+            uint8_t* gst = kGPrefetch ? qarea + (grp * kEpiChunks + ch) * 16384   // gate tile
+                                      : ring + 8192 + grp * 65536;
+            if (issuer) {
+                bulk_wait_read0();                                   // staging free again
+                if (EPI != 0 && !kGPrefetch && live) {
+                    mbar_arrive_expect_tx(&bars.g_full[grp], kGAtoms * 16384);
+                    for (int a2 = 0; a2 < kGAtoms; ++a2)
+                        tma_load_3d(gst + a2 * 16384, &mg, gcol + a2 * (EPI == 2 ? 64 : 32), n0, plane,
+                                    &bars.g_full[grp]);
                 }
             }
+            named_bar(6 + grp, 128);
+            bool got_g = true;
+            if (EPI != 0 && live) {
+                got_g = kGPrefetch ? __all_sync(0xffffffffu, mbar_wait(&bars.g_pre, 0, abort_p))
+                                   : __all_sync(0xffffffffu, mbar_wait(&bars.g_full[grp], ch & 1, abort_p));
+            }
+            if (live && got_g) {
+                float o[64];
+                tmem_ld32(tmem + lrow + kTO + kCols * grp + 64 * ch, o);
+                tmem_ld32(tmem + lrow + kTO + kCols * grp + 64 * ch + 32, o + 32);
+                float gv[64];
+                if (EPI == 2) {
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(gst + swz(c16));
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            gv[8 * c16 + 2 * e] = __uint_as_float(w4[e] << 16);
+                            gv[8 * c16 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                        }
+                    }
+                } else if (EPI == 1) {
+#pragma unroll
+                    for (int c16 = 0; c16 < 16; ++c16) {
+                        const float4 f = *reinterpret_cast<const float4*>(gst + (c16 / 8) * 16384 + swz(c16 % 8));
+                        gv[4 * c16] = f.x; gv[4 * c16 + 1] = f.y; gv[4 * c16 + 2] = f.z; gv[4 * c16 + 3] = f.w;
+                    }
+                }
+                tmem_wait_ld();
+                float* r = o;                                        // results replace O in place
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    if (EPI == 0) {
+                        r[j] = o[j] * inv;
+                    } else {
+                        float yn = (o[j] * inv - mean) * rstd;
+                        const int ch_ = head * dv + col + j;
+                        if (ea.weight) yn *= ea.weight[ch_];
+                        if (ea.bias) yn += ea.bias[ch_];
+                        // swish with the hardware exp2/reciprocal paths (a few ulp, far inside
+                        // the bf16-input tolerance); g -> -inf gives g * 0 = -0
+                        r[j] = __fdividef(gv[j], 1.0f + __expf(-gv[j])) * yn;
+                    }
+                }
+                if (OUT_BF16) {
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16)
+                        *reinterpret_cast<uint4*>(ost + swz(c16)) =
+                            make_uint4(pack_bf16(r[8 * c16], r[8 * c16 + 1]), pack_bf16(r[8 * c16 + 2], r[8 * c16 + 3]),
+                                       pack_bf16(r[8 * c16 + 4], r[8 * c16 + 5]), pack_bf16(r[8 * c16 + 6], r[8 * c16 + 7]));
+                } else {
+#pragma unroll
+                    for (int c16 = 0; c16 < 16; ++c16)
+                        *reinterpret_cast<float4*>(ost + (c16 / 8) * 16384 + swz(c16 % 8)) =
+                            make_float4(r[4 * c16], r[4 * c16 + 1], r[4 * c16 + 2], r[4 * c16 + 3]);
+                }
+            }
+            fence_proxy_async();
+            named_bar(6 + grp, 128);
+            if (issuer && live && got_g) {
+                for (int a2 = 0; a2 < kOutAtoms; ++a2)
+                    tma_store_3d(&mo, gcol + a2 * (OUT_BF16 ? 64 : 32), n0, plane, ost + a2 * 16384);
+                bulk_commit();
+            }
         }
+        if (issuer) bulk_wait0();
     }
     __syncwarp();
     tc_fence_before();
@@ -507,8 +548,9 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
 namespace {
 
-using ParKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, void*, int, int,
-                           int, int, int, int, unsigned, const ParConsts, const EpiArgs);
+using ParKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                           const CUtensorMap, const CUtensorMap, int, int, int, int, int, int,
+                           unsigned, const ParConsts, const EpiArgs);
 
 template <int EPI>
 ParKernel pick(int nh, int nv, int out_bf16) {
@@ -543,10 +585,19 @@ cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, 
     }
     const long long bH = (long long)b * H;
     if (bH >= (1LL << 31) || N >= (1 << 30)) return cudaErrorNotSupported;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo, mg;
     if (!make_map_bf16_3d(&mq, q, bH, N, dk, 128) || !make_map_bf16_3d(&mk, k, bH, N, dk, 128) ||
         !make_map_bf16_3d(&mv, v, bH, N, dv, 128))
         return cudaErrorInvalidValue;
+    // outputs (and the gate) move through 128-byte-wide boxes of 128 rows
+    if (epi == 0) {
+        if (!make_map_3d_128b(&mo, o, out_bf16 != 0, bH, N, dv, 128)) return cudaErrorInvalidValue;
+        mg = mo;
+    } else {
+        if (!make_map_3d_128b(&mo, o, out_bf16 != 0, b, N, (uint64_t)H * dv, 128) ||
+            !make_map_3d_128b(&mg, ea.g, epi == 2, b, N, (uint64_t)H * dv, 128))
+            return cudaErrorInvalidValue;
+    }
     const long long grid = (long long)((N + 127) / 128) * bH * nvb;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = (dk / 128) * kPiece + kRing * kPiece + 1024;
@@ -569,7 +620,7 @@ cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, o, N, H, dk, dv, (int)bH, nvb, flags, pc, ea);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mg, N, H, dk, dv, (int)bH, nvb, flags, pc, ea);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(epi == 0 ? RET_KERNEL_PARALLEL_TC : RET_KERNEL_PARALLEL_GATED_TC);
     return e;

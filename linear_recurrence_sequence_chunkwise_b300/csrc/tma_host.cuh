@@ -57,5 +57,23 @@ inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t planes
            CUDA_SUCCESS;
 }
 
+// Map over a bf16 or fp32 tensor [planes][rows][cols] whose boxes are 128 bytes wide
+// (64 bf16 or 32 fp32 columns) by box_rows rows, 128-byte swizzle; used for staged
+// epilogue loads and stores.
+inline bool make_map_3d_128b(CUtensorMap* map, const void* base, bool bf16, uint64_t planes,
+                             uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {cols, rows, planes};
+    cuuint64_t strides[2] = {cols * es, rows * cols * es};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 }  // namespace ret
