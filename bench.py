@@ -49,13 +49,16 @@ class Dist:
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
 
-    def init(self, backend: str | None = None):
+    def init(self, backend: str | None = None, timeout_s: float | None = None):
         if self.world > 1:
+            import datetime
+
             import torch.distributed as dist
             backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
             if torch.cuda.is_available():
                 torch.cuda.set_device(self.local)
-            dist.init_process_group(backend)
+            kw = {"timeout": datetime.timedelta(seconds=timeout_s)} if timeout_s else {}
+            dist.init_process_group(backend, **kw)
             self.pg = dist
         return self
 
