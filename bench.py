@@ -112,7 +112,7 @@ class Clocks:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -146,11 +146,14 @@ class Clocks:
         power = [float(r[3]) for r in rows if re.match(r"^[\d.]+$", r[3])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
-        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        # samples taken while the GPU drew load (power above the idle floor)
+        busy = [float(r[1]) for r in rows if re.match(r"^[\d.]+$", r[3]) and r[1].replace(".", "").isdigit()
+                and power and float(r[3]) > min(power) + 0.25 * (max(power) - min(power))]
+        loaded = busy or [s for s in sm if mx and s > 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "samples_under_load": len(busy), "reasons": reasons}
 
 
 def profile_traffic(summary_name: str, source_file: str):
@@ -434,7 +437,7 @@ def run_profile(case: str) -> int:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
