@@ -243,10 +243,11 @@ chunkwise_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
             auto wait_piece = [&](uint32_t f) { return wait(&bars.full[f % kStages], (f / kStages) & 1); };
             auto release_piece = [&](uint32_t f) { mma_commit(&bars.empty[f % kStages]); };
             // S(sb) = Q_rb K_cb^T  (M=128, N=128, K=dk), waiting for each dk half's pieces
-            // just before its k-steps; the buffer must have been read by its previous P.V.
+            // just before its k-steps.
             auto mma_s = [&](uint32_t base, int rb, int cb, int sb) {
                 uint32_t& su = sb ? s_use1 : s_use0;
-                if (su > 0) wait(&bars.pv_done[sb], (su - 1) & 1);
+                // the buffer's previous P.V (issued earlier by this thread) reads it before
+                // this MMA writes it: tcgen05.mma operations of one thread run in issue order
                 const uint32_t ts = tmem + kTS + 128 * sb;
                 for (int hh = 0; hh < nh && ok; ++hh) {
                     wait_piece(base + piece_index(0, rb, hh, nh));
