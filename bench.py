@@ -271,7 +271,7 @@ def bench_chunkwise(args, dist, rb, pk, out_dtype):
     peak = pk["bf16_tflops"]
     in_bytes = 2 * (2 * w.b * w.H * w.N * w.dk + w.b * w.H * w.N * w.dv)
     out_bytes = w.b * w.H * w.N * w.dv * (4 if out_dtype == "f32" else 2)
-    traffic = profile_traffic(f"chunkwise_tc_{w.name}.md", "tc_chunkwise.cu")
+    traffic = profile_traffic(f"chunkwise_tc_pair_{w.name}.md", "tc_chunkwise_pair.cu")
     res = {"value": value, "ms_per_step": ms_step, "launches": launches,
            "clocks": clk.summary(),
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -178,7 +178,8 @@ enum {
     RET_KERNEL_EPILOGUE = 4,        /* GroupNorm + swish gate                         */
     RET_KERNEL_CHUNKWISE_TC = 5,    /* chunkwise form, tcgen05 tensor-core kernel     */
     RET_KERNEL_PARALLEL_TC = 6,     /* parallel form, tcgen05 tensor-core kernel      */
-    RET_KERNEL_PARALLEL_GATED_TC = 7 /* parallel form + gated GroupNorm, tensor cores */
+    RET_KERNEL_PARALLEL_GATED_TC = 7, /* parallel form + gated GroupNorm, tensor cores */
+    RET_KERNEL_CHUNKWISE_TC_PAIR = 8  /* chunkwise form, tensor cores on pairs of SMs */
 };
 
 /*

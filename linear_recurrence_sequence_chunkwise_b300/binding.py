@@ -24,7 +24,7 @@ RET_F32, RET_BF16 = 0, 1
 NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
-                5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc"}
+                5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair"}
 
 _lib = None
 _lock = threading.Lock()

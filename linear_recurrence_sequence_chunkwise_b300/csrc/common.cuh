@@ -87,6 +87,11 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
                                 int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                 const HeadConsts& hc, const float* state_in, float* state_out,
                                 cudaStream_t s);
+// Pair-of-SMs chunkwise kernel (cta_group::2): chunk 256, dk 256, dv a multiple of 128.
+cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
+                                     int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
+                                     const HeadConsts& hc, const float* state_in, float* state_out,
+                                     cudaStream_t s);
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
                                int out_bf16, int b, int H, int N, int dk, int dv,
                                const HeadConsts& hc, unsigned flags, cudaStream_t s);
@@ -100,5 +105,6 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
 void count_launch(int kernel_code);
 // Device error words of the kernels with bounded waits: read and clear.
 unsigned read_clear_error_tc_chunkwise(cudaStream_t s);
+unsigned read_clear_error_tc_chunkwise_pair(cudaStream_t s);
 unsigned read_clear_error_tc_parallel(cudaStream_t s);
 }  // namespace ret

@@ -160,8 +160,11 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int ob = out_dtype == RET_BF16;
     if (in_dtype == RET_BF16) {
-        cudaError_t e = ret::launch_chunkwise_tc(q, k, v, o, ob, b, H, N, dk, dv, chunk, hc,
-                                                 state_in, state_out, s);
+        cudaError_t e = ret::launch_chunkwise_tc_pair(q, k, v, o, ob, b, H, N, dk, dv, chunk, hc,
+                                                      state_in, state_out, s);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+        e = ret::launch_chunkwise_tc(q, k, v, o, ob, b, H, N, dk, dv, chunk, hc, state_in,
+                                     state_out, s);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     return cuda_status(ret::launch_chunkwise_simt(q, k, v, o, in_dtype == RET_BF16, ob, b, H, N,
@@ -221,7 +224,8 @@ int retention_check_device_error(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce = cudaStreamSynchronize(s);
     if (ce != cudaSuccess) return cuda_status(ce);
-    unsigned e = ret::read_clear_error_tc_chunkwise(s) | ret::read_clear_error_tc_parallel(s);
+    unsigned e = ret::read_clear_error_tc_chunkwise(s) | ret::read_clear_error_tc_chunkwise_pair(s) |
+                 ret::read_clear_error_tc_parallel(s);
     ce = cudaGetLastError();
     if (ce != cudaSuccess) return cuda_status(ce);
     return e ? RET_ERR_TIMEOUT : RET_OK;

@@ -1,0 +1,606 @@
+// tc_chunkwise_pair.cu -- chunkwise recurrent retention on pairs of SMs (tcgen05 cta_group::2).
+//
+// Computes eq.(7) of "Transformer取代者登場！…RetNet…（2）", section "Retention" 3), the same
+// function as tc_chunkwise.cu:
+//     O[iB+j] = sum_{r<=j} (q_j.k_r) g^(j-r) v_r + g^(j+1) (q_j R_{i-1})
+//     R_i     = sum_r g^(B-1-r) k_r^T v_r + g^B R_{i-1}
+// for bf16 Q/K/V, fp32 accumulation and state, chunk B = 256, dk = 256, dv a multiple of
+// 128.  Decay folding and the hi/lo bf16 split of the state copy and of the scores are
+// those of tc_chunkwise.cu (Vz = zeta (.) V, P = g^(-B) S (.) M, xi_j applied to the
+// output rows, R <- g^B R then R += K^T Vz).
+//
+// Work split: one cluster of two CTAs (the two SMs of a pair) per (batch*head, 128-column
+// block of dv); the even CTA issues every MMA as a pair MMA (M = 256, 128 rows per SM):
+//   S  = Q K^T        M = 256 query rows of the chunk (CTA r: rows 128r..), N = 256 keys
+//                     (B operand split: CTA r holds keys 128r..), K = dk
+//   O  = Q R_{i-1}    N = 128 value columns (B split: CTA r holds the bf16 hi/lo copy of
+//                     R[:, 64r..64r+63]), K = dk, as two MMAs (hi, lo)
+//   R += K^T Vz       M = 256 dk rows (CTA r: dk 128r..; the state lives in tensor memory,
+//                     split by dk), N = 128 value columns, K = 256 keys
+//   O += P Vz         A = P from tensor memory (hi and lo), N = 128, K = 256 keys
+// Every MMA has N >= 128 per SM, and each SM reads only its half of each B operand, so
+// the tensor pipe runs at full rate with half the shared-memory operand traffic of the
+// one-SM split into 64-column blocks, and the score tile of a head is computed by dv/128
+// pairs instead of dv/64 CTAs.  The pair costs one duplicated quarter of the score tile
+// (the even CTA's rows against keys 128-255, all masked) and of P.V.
+//
+// Roles (320 threads per CTA): warp 0 issues this CTA's TMA loads (Q, K and the K^T
+// operand complete on the even CTA's barriers, V on a local one), warp 1 allocates
+// tensor memory (both CTAs, collectively) and, in the even CTA, issues the MMAs, warps
+// 2-5 turn this CTA's score rows into P and then write its output rows (staged in shared
+// memory, TMA stores), warps 6-9 copy and rescale this CTA's state rows (writing the
+// hi/lo copy into both CTAs' shared memory) and scale V.  Warp w reaches TMEM lanes
+// 32*(w%4)..+31.  Every wait is bounded;
+// a wait that gives up sets the device error word and both CTAs' abort flags, and the
+// CTAs unwind, meet at a final cluster barrier and free their tensor memory.
+//
+// Tensor memory per CTA (512 columns x 128 lanes, fp32):
+//   [  0,256) S: this CTA's 128 query rows x 256 keys; P written in place as bf16 pairs
+//             (per 32 keys: 16 columns of hi pairs, then 16 of lo pairs)
+//   [256,384) O: this CTA's 128 query rows x 128 value columns
+//   [384,512) R: this CTA's 128 dk rows of the state x 128 value columns
+// Shared memory per CTA (1024-aligned, 224 KB), each box 128 rows x 64 bf16, 128B swizzle:
+//   Q   64 KB  own 128 query rows x 4 dk boxes
+//   K   64 KB  own 128 keys x 4 dk boxes (S); after S the K^T operand of the state update:
+//              all 256 keys x own 128 dk columns (2 dk boxes x 2 key blocks)
+//   V   32 KB  256 keys x own 64 value columns (scaled in place to Vz); once P.Vz has
+//              completed, the staging area of the output tiles (TMA stores)
+//   Rhi 32 KB, Rlo 32 KB  bf16 copy of R_{i-1}: 256 dk rows x own 64 columns
+// MMA order in a chunk: S, Q.R, K^T.Vz, P.Vz; the K area is reloaded with the K^T operand
+// during Q.R and with the next chunk's keys during P.Vz.
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace ret {
+namespace {
+
+__device__ unsigned g_err_chunkwise_pair;
+
+using namespace tc;
+
+constexpr int kThreads = 320;
+constexpr int kB = 256;                        // chunk length
+constexpr int kDk = 256;
+constexpr int kBox = 128 * 128;                // 128 rows x 64 bf16
+constexpr int kQOff = 0;
+constexpr int kKOff = kQOff + 4 * kBox;
+constexpr int kVOff = kKOff + 4 * kBox;
+constexpr int kRhiOff = kVOff + 2 * kBox;
+constexpr int kRloOff = kRhiOff + 2 * kBox;
+constexpr int kSmemBytes = kRloOff + 2 * kBox;  // 229376
+constexpr uint32_t kTS = 0, kTO = 256, kTR = 384;
+constexpr uint32_t kPairArrivals = 8;          // 4 warps in each CTA
+constexpr uint16_t kBoth = 3;                  // multicast mask: both CTAs of the pair
+constexpr int kStoreWarp = 2;                  // its lane 0 issues the output TMA stores
+
+struct Decay {
+    float l2g[kMaxHeads];   // log2(gamma)
+    float gB[kMaxHeads];    // gamma^B
+    float cP[kMaxHeads];    // gamma^(-B)
+};
+
+struct Bars {
+    // the even CTA's copies count both CTAs' work
+    uint64_t q_full, k_full, kt_full;              // pair loads (transaction bytes)
+    uint64_t vz_ready, p_ready, rcopy, o_free;     // 8 warp arrivals
+    // each CTA's own copy, arrived on by the MMA commits (multicast)
+    uint64_t q_empty, k_empty, kt_empty;
+    uint64_t s_full, o_full, r_done;
+    uint64_t v_full;                               // local V load
+    uint64_t stage_written, stage_read;            // output staging rounds in the V area
+    uint64_t stage_free;                           // a chunk's output has left the V area
+    uint64_t drain;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(x0, x1);
+    lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
+}
+
+template <bool OUT_BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                      const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                      const float* __restrict__ state_in, float* __restrict__ state_out, int N,
+                      int H, int dv, const Decay dc) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sq = sm + kQOff;
+    uint8_t* sk = sm + kKOff;
+    uint8_t* sv = sm + kVOff;
+    uint8_t* rhi = sm + kRhiOff;
+    uint8_t* rlo = sm + kRloOff;
+    __shared__ Bars bars;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const int nblk = dv / 128;
+    const int pair = (int)(blockIdx.x >> 1);
+    const int bh = pair / nblk, blk = pair % nblk;
+    const int head = bh % H;
+    const int nchunks = N / kB;
+    constexpr int kOutRounds = OUT_BF16 ? 1 : 2;   // 32 KB staging rounds per 128 output columns
+    volatile int* abort_p = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full, 1); mbar_init(&bars.kt_full, 1);
+        mbar_init(&bars.vz_ready, kPairArrivals); mbar_init(&bars.p_ready, kPairArrivals);
+        mbar_init(&bars.rcopy, kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
+        mbar_init(&bars.q_empty, 1); mbar_init(&bars.k_empty, 1);
+        mbar_init(&bars.kt_empty, 1);
+        mbar_init(&bars.s_full, 1); mbar_init(&bars.o_full, 1); mbar_init(&bars.r_done, 1);
+        mbar_init(&bars.v_full, 1); mbar_init(&bars.drain, 1);
+        mbar_init(&bars.stage_written, 4); mbar_init(&bars.stage_read, 1);
+        mbar_init(&bars.stage_free, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) { tmem_alloc_pair(&tmem_slot, 512); tmem_relinquish_pair(); }
+    tc_fence_before();
+    cluster_sync_all();     // both CTAs' barriers exist before any remote arrive or pair load
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t peer_abort = map_peer(&abort_flag, peer);
+    auto fail = [&]() {
+        *abort_p = 1;
+        st_cluster_s32(peer_abort, 1);
+        atomicOr(&g_err_chunkwise_pair, 1u);
+    };
+    auto lead = [&](uint64_t* b) { return map_peer(b, 0); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv);
+            tma_prefetch_desc(&mo);
+            const uint32_t qf = lead(&bars.q_full), kf = lead(&bars.k_full), ktf = lead(&bars.kt_full);
+            const int rowbase = bh * N;
+            const int own = 128 * (int)rank, other = 128 * (int)peer;
+            const int vcol = blk * 128 + 64 * (int)rank;
+            uint32_t armed_q = 0, armed_k = 0, armed_kt = 0, v_loads = 0;
+            bool ok = true;
+            auto w = [&](uint64_t* bar, uint32_t par) {
+                if (ok && !mbar_wait(bar, par, abort_p)) { ok = false; fail(); }
+                return ok;
+            };
+            // the pairs of one head share Q and K: pull the next chunk's boxes into L2
+            auto prefetch = [&](int c) {
+                if (c >= nchunks) return;
+                const int r0 = rowbase + c * kB;
+                for (int a = 0; a < 4; ++a) {
+                    tma_prefetch_l2(&mq, 64 * a, r0 + own);
+                    tma_prefetch_l2(&mk, 64 * a, r0 + own);
+                }
+                for (int m = 0; m < 2; ++m) tma_prefetch_l2(&mk, 64 * (2 * (int)rank + m), r0 + other);
+                for (int j = 0; j < 2; ++j) tma_prefetch_l2(&mv, vcol, r0 + 128 * j);
+            };
+            prefetch(0);
+            for (int c = 0; c < nchunks && ok; ++c) {
+                prefetch(c + 1);
+                const int r0 = rowbase + c * kB;
+                // Q: own query rows, all dk (after the previous chunk's Q.R)
+                if (c > 0 && !w(&bars.q_empty, (c - 1) & 1)) break;
+                if (rank == 0) { mbar_arrive_expect_tx(&bars.q_full, 2 * 4 * kBox); ++armed_q; }
+                for (int a = 0; a < 4; ++a) tma_load_2d_pair(sq + a * kBox, &mq, 64 * a, r0 + own, qf);
+                // K: own keys, all dk (after the previous chunk's K^T.Vz)
+                if (c > 0 && !w(&bars.kt_empty, (c - 1) & 1)) break;
+                if (rank == 0) { mbar_arrive_expect_tx(&bars.k_full, 2 * 4 * kBox); ++armed_k; }
+                for (int a = 0; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf);
+                // V: all keys of the chunk, own 64 value columns, once the previous chunk's
+                // output tiles have left the V area (one completion per chunk: a parity wait
+                // never runs more than one phase behind)
+                if (c > 0 && !w(&bars.stage_free, (uint32_t)(c - 1) & 1u)) break;
+                mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
+                for (int j = 0; j < 2; ++j) tma_load_2d(sv + j * kBox, &mv, vcol, r0 + 128 * j, &bars.v_full);
+                ++v_loads;
+                // K^T operand: all keys, own dk half; box (m, j) = dk box 2*rank+m of key
+                // block j, placed so that each dk box holds keys 0..255 in order
+                if (!w(&bars.k_empty, c & 1)) break;
+                if (rank == 0) { mbar_arrive_expect_tx(&bars.kt_full, 2 * 4 * kBox); ++armed_kt; }
+                for (int m = 0; m < 2; ++m)
+                    for (int j = 0; j < 2; ++j)
+                        tma_load_2d_pair(sk + (2 * m + j) * kBox, &mk, 64 * (2 * (int)rank + m),
+                                         r0 + 128 * j, ktf);
+            }
+            if (!ok) {
+                // let loads in flight land before the CTAs unwind
+                if (v_loads) mbar_wait(&bars.v_full, (v_loads - 1) & 1, nullptr, 100000000ull);
+                if (rank == 0) {
+                    if (armed_q) mbar_wait(&bars.q_full, (armed_q - 1) & 1, nullptr, 100000000ull);
+                    if (armed_k) mbar_wait(&bars.k_full, (armed_k - 1) & 1, nullptr, 100000000ull);
+                    if (armed_kt) mbar_wait(&bars.kt_full, (armed_kt - 1) & 1, nullptr, 100000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (rank == 0 && lane == 0) {
+            const uint32_t id_s = idesc_bf16(256, 256, 0, 0);    // Q K^T: both K-major
+            const uint32_t id_q = idesc_bf16(256, 128, 0, 1);    // Q R: B MN-major
+            const uint32_t id_r = idesc_bf16(256, 128, 1, 1);    // K^T Vz: both MN-major
+            const uint32_t id_p = idesc_bf16(256, 128, 0, 1);    // P Vz: A in TMEM, B MN-major
+            // descriptors are linear in the start address: base descriptor + offset / 16
+            const uint64_t dQ = sdesc_sw128(smem_u32(sq), 16, 1024);
+            const uint64_t dK = sdesc_sw128(smem_u32(sk), 16, 1024);
+            const uint64_t dKT = sdesc_sw128(smem_u32(sk), 2 * kBox, 1024);  // dk boxes 32 KB apart
+            const uint64_t dV = sdesc_sw128(smem_u32(sv), 2 * kBox, 1024);
+            const uint64_t dRhi = sdesc_sw128(smem_u32(rhi), 2 * kBox, 1024);
+            const uint64_t dRlo = sdesc_sw128(smem_u32(rlo), 2 * kBox, 1024);
+            bool ok = true;
+            auto w = [&](uint64_t* bar, uint32_t par) {
+                if (ok && !mbar_wait_cl(bar, par, abort_p)) { ok = false; fail(); }
+                return ok;
+            };
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const uint32_t ph = (uint32_t)c & 1u;
+                // S = Q K^T (the previous P.Vz, issued earlier, reads the S columns first:
+                // tcgen05.mma operations of one thread run in issue order)
+                if (!w(&bars.q_full, ph) || !w(&bars.k_full, ph)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t off = (uint64_t)((a * kBox + kk * 32) >> 4);
+                        mma_pair(tmem + kTS, dQ + off, dK + off, id_s, (a | kk) != 0);
+                    }
+                mma_commit_pair(&bars.s_full, kBoth);
+                mma_commit_pair(&bars.k_empty, kBoth);
+                // O = Q (R_hi + R_lo); the first MMA overwrites the accumulator
+                if (!w(&bars.rcopy, ph)) break;
+                if (c > 0 && !w(&bars.o_free, (c - 1) & 1)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t qa = dQ + (uint64_t)((a * kBox + kk * 32) >> 4);
+                        const uint64_t ro = (uint64_t)(((4 * a + kk) * 2048) >> 4);
+                        mma_pair(tmem + kTO, qa, dRhi + ro, id_q, (a | kk) != 0);
+                        mma_pair(tmem + kTO, qa, dRlo + ro, id_q, 1);
+                    }
+                mma_commit_pair(&bars.q_empty, kBoth);
+                // R += K^T Vz (R was rescaled by g^B with the copy)
+                if (!w(&bars.kt_full, ph) || !w(&bars.vz_ready, ph)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint64_t off = (uint64_t)((t * 2048) >> 4);
+                    mma_pair(tmem + kTR, dKT + off, dV + off, id_r, 1);
+                }
+                mma_commit_pair(&bars.kt_empty, kBoth);
+                mma_commit_pair(&bars.r_done, kBoth);
+                // O += (P_hi + P_lo) Vz
+                if (!w(&bars.p_ready, ph)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint32_t a_hi = tmem + kTS + 32 * (t >> 1) + 8 * (t & 1);
+                    const uint64_t bd = dV + (uint64_t)((t * 2048) >> 4);
+                    mma_pair_ts(tmem + kTO, a_hi, bd, id_p, 1);
+                    mma_pair_ts(tmem + kTO, a_hi + 16, bd, id_p, 1);
+                }
+                mma_commit_pair(&bars.o_full, kBoth);
+            }
+            // every issued MMA completes before tensor memory is released
+            mma_commit_pair(&bars.drain, 1);
+            mbar_wait(&bars.drain, 0, nullptr, 200000000ull);
+        }
+    } else {
+        // ------------------------------------------------------------ transform warps
+        const bool pwarp = warp < 6;                 // warps 2-5: scores; 6-9: state/V/out
+        const int q4 = warp & 3;                     // TMEM lane quarter of this warp
+        const int row = 32 * q4 + lane;              // TMEM lane
+        const uint32_t lrow = (uint32_t)(32 * q4) << 16;
+        const int j = 128 * (int)rank + row;         // query row in the chunk / dk row of R
+        const float l2g = dc.l2g[head];
+        bool ok = true;
+        // tcgen05.ld/st are warp-collective: keep the outcome of every wait uniform
+        auto wait = [&](uint64_t* bar, uint32_t par) {
+            if (!ok) return false;
+            const bool got = __all_sync(0xffffffffu, mbar_wait(bar, par, abort_p));
+            if (!got) { ok = false; if (lane == 0) fail(); }
+            return ok;
+        };
+        auto arrive_lead = [&](uint64_t* bar) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cl(lead(bar));
+        };
+        // output rows of chunk c: xi_j * O, staged as 128-byte-swizzled boxes (128 rows x
+        // 128 bytes) in the V area, which P.Vz no longer reads once o_full completed, and
+        // written by TMA stores: two boxes per round, 128 columns in kOutRounds rounds
+        auto do_out = [&](int c) {
+            if (!wait(&bars.o_full, (uint32_t)c & 1u)) return;
+            tc_fence_after();
+            const float xi = exp2f(l2g * (float)(j + 1));
+            const int orow0 = bh * N + c * kB + 128 * (int)rank;
+            constexpr int kBoxCols = OUT_BF16 ? 64 : 32;
+#pragma unroll 1
+            for (int rr = 0; rr < kOutRounds; ++rr) {
+                const uint32_t n = (uint32_t)(c * kOutRounds + rr);   // staging round
+                if (rr > 0 && !wait(&bars.stage_read, (n - 1) & 1u)) return;
+#pragma unroll 1
+                for (int bx = 0; bx < 2; ++bx) {
+                    const uint32_t col0 = (uint32_t)((2 * rr + bx) * kBoxCols);
+                    uint8_t* srow = sv + bx * kBox + row * 128;
+                    if (OUT_BF16) {
+                        float o[64];
+                        tmem_ld32(tmem + lrow + kTO + col0, o);
+                        tmem_ld32(tmem + lrow + kTO + col0 + 32, o + 32);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc)
+                            *reinterpret_cast<uint4*>(srow + (((uint32_t)cc ^ ((uint32_t)row & 7u)) << 4)) =
+                                make_uint4(pack_bf16(xi * o[8 * cc], xi * o[8 * cc + 1]),
+                                           pack_bf16(xi * o[8 * cc + 2], xi * o[8 * cc + 3]),
+                                           pack_bf16(xi * o[8 * cc + 4], xi * o[8 * cc + 5]),
+                                           pack_bf16(xi * o[8 * cc + 6], xi * o[8 * cc + 7]));
+                    } else {
+                        float o[32];
+                        tmem_ld32(tmem + lrow + kTO + col0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc)
+                            *reinterpret_cast<float4*>(srow + (((uint32_t)cc ^ ((uint32_t)row & 7u)) << 4)) =
+                                make_float4(xi * o[4 * cc], xi * o[4 * cc + 1], xi * o[4 * cc + 2],
+                                            xi * o[4 * cc + 3]);
+                    }
+                }
+                if (rr == kOutRounds - 1) {
+                    tc_fence_before();
+                    arrive_lead(&bars.o_free);       // O read out: the next Q.R may overwrite it
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.stage_written);
+                if (warp == kStoreWarp) {
+                    bool good = true;
+                    if (lane == 0) {
+                        good = mbar_wait(&bars.stage_written, n & 1u, abort_p);
+                        if (good) {
+                            for (int bx = 0; bx < 2; ++bx)
+                                tma_store_3d(&mo, blk * 128 + (2 * rr + bx) * kBoxCols, orow0, 0,
+                                             sv + bx * kBox);
+                            bulk_commit();
+                            bulk_wait_read0();
+                            mbar_arrive(&bars.stage_read);
+                            if (rr == kOutRounds - 1) mbar_arrive(&bars.stage_free);
+                        } else {
+                            fail();
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) { ok = false; return; }
+                }
+            }
+        };
+        if (pwarp) {
+            const float cP = dc.cP[head];
+            // P = g^(-B) S with the causal mask (key > j is zero), as hi/lo bf16 pairs in place.
+            // Key quarter qq (32 keys) is below this warp's rows for qq < dq, holds their
+            // diagonal for qq = dq and lies after them for qq > dq (all zero): warp-uniform.
+            const int dq = 4 * (int)rank + q4;
+            auto convert = [&](const float* x, int qq, uint32_t* pp) {
+                if (qq < dq) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) split2(x[2 * e] * cP, x[2 * e + 1] * cP, pp[e], pp[16 + e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int kc = 32 * qq + 2 * e;
+                        const float x0 = kc > j ? 0.f : x[2 * e] * cP;
+                        const float x1 = kc + 1 > j ? 0.f : x[2 * e + 1] * cP;
+                        split2(x0, x1, pp[e], pp[16 + e]);
+                    }
+                }
+            };
+            for (int c = 0; c < nchunks && ok; ++c) {
+                if (!wait(&bars.s_full, (uint32_t)c & 1u)) break;
+                tc_fence_after();
+                // two quarters per step: both loads in flight before either is converted
+#pragma unroll 1
+                for (int qq = 0; qq <= dq; qq += 2) {
+                    const bool two = qq + 1 <= dq;
+                    const uint32_t ts = tmem + lrow + kTS + 32 * qq;
+                    float x[64];
+                    uint32_t pp[32];
+                    tmem_ld32(ts, x);
+                    if (two) tmem_ld32(ts + 32, x + 32);
+                    tmem_wait_ld();
+                    convert(x, qq, pp);
+                    tmem_st32(ts, reinterpret_cast<const float*>(pp));
+                    if (two) {
+                        convert(x + 32, qq + 1, pp);
+                        tmem_st32(ts + 32, reinterpret_cast<const float*>(pp));
+                    }
+                }
+                {
+                    uint32_t zz[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) zz[e] = 0u;
+#pragma unroll 1
+                    for (int qq = dq + 1; qq < 8; ++qq)
+                        tmem_st32(tmem + lrow + kTS + 32 * qq, reinterpret_cast<const float*>(zz));
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                arrive_lead(&bars.p_ready);
+                // this chunk's output once its last P.Vz completed
+                do_out(c);
+            }
+            if (warp == kStoreWarp && lane == 0) bulk_wait0();   // output stores complete
+        } else {
+            const float gB = dc.gB[head];
+            const uint32_t hi_local = smem_u32(rhi) + (uint32_t)j * 128u;
+            const uint32_t lo_local = smem_u32(rlo) + (uint32_t)j * 128u;
+            const uint32_t hi_peer = map_peer(rhi, peer) + (uint32_t)j * 128u;
+            const uint32_t lo_peer = map_peer(rlo, peer) + (uint32_t)j * 128u;
+            // state: hi/lo copy of R_{i-1} (this CTA's dk row j, all 128 columns; columns
+            // 64r.. go to CTA r), then R <- g^B R in TMEM
+            auto do_state = [&](int c) {
+                if (c > 0) {
+                    if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
+                    tc_fence_after();
+                }
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    const uint32_t tcol = tmem + lrow + kTR + 32 * g;
+                    float x[32];
+                    if (c == 0) {
+                        if (state_in) {
+                            const float4* src = reinterpret_cast<const float4*>(
+                                state_in + ((size_t)bh * kDk + j) * dv + blk * 128 + 32 * g);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 f = src[e];
+                                x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) x[e] = 0.f;
+                        }
+                    } else {
+                        tmem_ld32(tcol, x);
+                        tmem_wait_ld();
+                    }
+                    const bool local = (uint32_t)(g >> 1) == rank;
+                    const uint32_t hb = local ? hi_local : hi_peer;
+                    const uint32_t lb = local ? lo_local : lo_peer;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t h[4], l[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], h[e], l[e]);
+                        const uint32_t chunk = (uint32_t)(4 * (g & 1) + cc);
+                        const uint32_t off = ((chunk ^ ((uint32_t)j & 7u)) << 4);
+                        if (local) {
+                            *reinterpret_cast<uint4*>(rhi + j * 128 + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<uint4*>(rlo + j * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
+                        } else {
+                            st_cluster_v4(hb + off, h[0], h[1], h[2], h[3]);
+                            st_cluster_v4(lb + off, l[0], l[1], l[2], l[3]);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] *= gB;
+                    tmem_st32(tcol, x);
+                }
+                tmem_wait_st();
+                fence_proxy_async_cluster();
+                tc_fence_before();
+                arrive_lead(&bars.rcopy);
+            };
+            // V rows kr = row and 128 + row of the chunk, scaled by g^(B-1-kr)
+            auto do_v = [&](int c) {
+                if (!wait(&bars.v_full, (uint32_t)c & 1u)) return;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int kr = 128 * half + row;
+                    const float f = exp2f(l2g * (float)(kB - 1 - kr));
+                    uint8_t* vrow = sv + kr * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint4* p = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
+                        uint4 u = *p;
+                        uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16(bf16_lo(wv[e]) * f, bf16_hi(wv[e]) * f);
+                        *p = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+                fence_proxy_async();
+                arrive_lead(&bars.vz_ready);
+            };
+            for (int c = 0; c < nchunks && ok; ++c) {
+                do_state(c);
+                do_v(c);
+            }
+            // ---- final state: this CTA's dk rows of R_{N/B-1}
+            if (ok && state_out && nchunks > 0) {
+                if (wait(&bars.r_done, (uint32_t)(nchunks - 1) & 1u)) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int g = 0; g < 4; ++g) {
+                        float x[32];
+                        tmem_ld32(tmem + lrow + kTR + 32 * g, x);
+                        tmem_wait_ld();
+                        float4* dst = reinterpret_cast<float4*>(
+                            state_out + ((size_t)bh * kDk + j) * dv + blk * 128 + 32 * g);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();     // no MMA in flight, no remote access pending
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool chunkwise_pair_supported(int dk, int dv, int chunk, const HeadConsts& hc, int H) {
+    if (dk != kDk || chunk != kB || dv % 128 != 0) return false;
+    for (int h = 0; h < H; ++h)
+        if (!(hc.l2g[h] * (float)chunk >= -64.0f)) return false;   // g^(-B) <= 2^64
+    return true;
+}
+
+cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
+                                     int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
+                                     const HeadConsts& hc, const float* state_in, float* state_out,
+                                     cudaStream_t s) {
+    if (!chunkwise_pair_supported(dk, dv, chunk, hc, H)) return cudaErrorNotSupported;
+    Decay dc;
+    for (int h = 0; h < H; ++h) {
+        dc.l2g[h] = hc.l2g[h];
+        dc.gB[h] = hc.gB[h];
+        dc.cP[h] = hc.ginvB[h];
+    }
+    const long long rows = (long long)b * H * N;
+    if (rows >= (1LL << 31)) return cudaErrorNotSupported;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map_bf16(&mq, q, rows, dk, 128) || !make_map_bf16(&mk, k, rows, dk, 128) ||
+        !make_map_bf16(&mv, v, rows, dv, 128) ||
+        !make_map_3d_128b(&mo, o, out_bf16 != 0, 1, rows, dv, 128))
+        return cudaErrorInvalidValue;
+    const long long grid = 2LL * b * H * (dv / 128);
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int smem = kSmemBytes + 1024;
+    auto kern = out_bf16 ? chunkwise_pair_kernel<true> : chunkwise_pair_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, mo, state_in, state_out, N, H, dv, dc);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
+    return e;
+}
+
+unsigned read_clear_error_tc_chunkwise_pair(cudaStream_t s) {
+    unsigned h = 0, z = 0;
+    if (cudaMemcpyFromSymbolAsync(&h, g_err_chunkwise_pair, sizeof(h), 0, cudaMemcpyDeviceToHost,
+                                  s) != cudaSuccess)
+        return 0;
+    cudaMemcpyToSymbolAsync(g_err_chunkwise_pair, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s);
+    cudaStreamSynchronize(s);
+    return h;
+}
+
+}  // namespace ret

@@ -43,6 +43,12 @@ def err_bf16_out(got, want):
     return float(np.max(np.abs(g - w) / (TOL_BF16 * rms + 2.0 ** -8 * np.abs(w))))
 
 
+def chunkwise_tc_name(dk, dv, chunk):
+    """Tensor-core chunkwise kernel the library picks for bf16 inputs of this shape:
+    the pair-of-SMs kernel for chunk 256, dk 256, dv a multiple of 128."""
+    return "chunkwise_tc_pair" if (chunk == 256 and dk == 256 and dv % 128 == 0) else "chunkwise_tc"
+
+
 def guarded(shape, dtype, device, pad=64):
     """A tensor view with `pad` sentinel elements on each side (canary guard bands)."""
     n = int(np.prod(shape))

@@ -38,7 +38,7 @@ def test_chunkwise_long_full():
     out = rb.retention_chunkwise(q, k, v, w.gamma, w.chunk)
     kern = rb.last_kernel()
     rb.check_device_error()
-    assert kern == "chunkwise_tc"
+    assert kern == "chunkwise_tc_pair"
     assert torch.isfinite(out).all()
     idx = [(0, 0), (0, 15)]
     us = units_of(q, k, v, idx)

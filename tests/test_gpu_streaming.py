@@ -12,7 +12,7 @@ import oracle
 from linear_recurrence_sequence_chunkwise_b300 import binding as rb
 from linear_recurrence_sequence_chunkwise_b300 import inputs, streaming
 
-from _util import TOL_BF16, err_bf16, err_f32
+from _util import TOL_BF16, chunkwise_tc_name, err_bf16, err_f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -42,7 +42,7 @@ def test_streamed_equals_single_call(dk, dv, chunk, seg):
     ho.fill_(float("nan"))
     streaming.chunkwise_from_host(hq, hk, hv, g, chunk, ho, seg)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == "chunkwise_tc"
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
     one = rb.retention_chunkwise(hq.to(DEV), hk.to(DEV), hv.to(DEV), g, chunk).cpu()
     assert not torch.isnan(ho).any()
     assert err_f32(ho, one) < 1e-5

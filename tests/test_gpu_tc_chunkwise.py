@@ -12,7 +12,7 @@ import oracle
 from linear_recurrence_sequence_chunkwise_b300 import binding as rb
 from linear_recurrence_sequence_chunkwise_b300 import inputs
 
-from _util import TOL_BF16, err_bf16, err_bf16_out, err_f32
+from _util import TOL_BF16, chunkwise_tc_name, err_bf16, err_bf16_out, err_f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -33,13 +33,14 @@ def mk(b, H, N, dk, dv, seed, std=1 / 16):
 
 
 @pytest.mark.parametrize("chunk", [128, 256])
-@pytest.mark.parametrize("dk,dv", [(256, 512), (128, 64), (256, 192), (128, 128)])
+@pytest.mark.parametrize("dk,dv", [(256, 512), (128, 64), (256, 192), (128, 128), (256, 128),
+                                   (256, 384)])
 def test_tc_chunkwise_shapes(chunk, dk, dv):
     b, H, N = 2, 2, 1024
     q, k, v = mk(b, H, N, dk, dv, 100 + dk + dv)
     g = [0.96875, 0.9990234375]
     got = rb.retention_chunkwise(q, k, v, g, chunk)
-    assert rb.last_kernel() == "chunkwise_tc"
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
     rb.check_device_error()
 
@@ -51,8 +52,20 @@ def test_tc_chunkwise_decay_range(chunk):
     q, k, v = mk(b, H, N, dk, dv, 200)
     g = [0.71 if chunk == 128 else 0.845, 0.9, 0.999, 1.0 - 2.0 ** -20]
     got = rb.retention_chunkwise(q, k, v, g, chunk)
-    assert rb.last_kernel() == "chunkwise_tc"
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
+
+
+@pytest.mark.parametrize("dv", [128, 512])
+def test_tc_chunkwise_pair_decay_range(dv):
+    """The pair kernel from the smallest decay the folded factors allow to almost 1."""
+    b, H, N, dk = 1, 4, 768, 256
+    q, k, v = mk(b, H, N, dk, dv, 250 + dv)
+    g = [0.845, 0.9, 0.999, 1.0 - 2.0 ** -20]
+    got = rb.retention_chunkwise(q, k, v, g, 256)
+    assert rb.last_kernel() == "chunkwise_tc_pair"
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, 256)) < TOL_BF16
+    rb.check_device_error()
 
 
 def test_tc_chunkwise_unit_scale_inputs():
@@ -80,7 +93,7 @@ def test_tc_chunkwise_states_and_bf16_out(chunk):
                                             v[:, :, sl].contiguous(), g, chunk,
                                             state_in=st if lo else None, state_out=st,
                                             out_dtype=torch.bfloat16))
-        assert rb.last_kernel() == "chunkwise_tc"
+        assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
     assert err_bf16_out(torch.cat(parts, dim=2), want) < 1.0
     assert err_f32(st, s_end) < TOL_BF16
 
@@ -108,11 +121,11 @@ def test_small_decay_uses_cuda_core_kernel(chunk, gmin):
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
 
 
-@pytest.mark.parametrize("chunk", [128, 256])
-def test_tc_chunkwise_repeatable_and_guarded(chunk):
+@pytest.mark.parametrize("chunk,dv", [(128, 192), (256, 192), (256, 384)])
+def test_tc_chunkwise_repeatable_and_guarded(chunk, dv):
     """Two calls give bit-identical results; guard bands around O stay intact."""
     from _util import guarded, guards_intact
-    b, H, N, dk, dv = 1, 3, 512, 256, 192
+    b, H, N, dk = 1, 3, 512, 256
     q, k, v = mk(b, H, N, dk, dv, 700)
     g = inputs.gammas(H)
     buf, o = guarded((b, H, N, dv), torch.float32, DEV)
@@ -120,7 +133,7 @@ def test_tc_chunkwise_repeatable_and_guarded(chunk):
     first = o.clone()
     rb.retention_chunkwise(q, k, v, g, chunk, out=o)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == "chunkwise_tc"
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
     assert torch.equal(first, o)
     assert guards_intact(buf)
     assert err_bf16(o, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
