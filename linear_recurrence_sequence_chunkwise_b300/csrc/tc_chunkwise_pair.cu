@@ -24,13 +24,13 @@
 // pairs instead of dv/64 CTAs.  The pair costs one duplicated quarter of the score tile
 // (the even CTA's rows against keys 128-255, all masked) and of P.V.
 //
-// Roles (320 threads per CTA): warp 0 issues this CTA's TMA loads (Q, K and the K^T
+// Roles (384 threads per CTA): warp 0 issues this CTA's TMA loads (Q, K and the K^T
 // operand complete on the even CTA's barriers, V on a local one), warp 1 allocates
 // tensor memory (both CTAs, collectively) and, in the even CTA, issues the MMAs, warps
-// 2-5 turn this CTA's score rows into P and then write its output rows (staged in shared
-// memory, TMA stores), warps 6-9 copy and rescale this CTA's state rows (writing the
-// hi/lo copy into both CTAs' shared memory) and scale V.  Warp w reaches TMEM lanes
-// 32*(w%4)..+31.  Every wait is bounded;
+// 2-5 turn this CTA's score rows into P and then write its output rows (coalesced stores
+// from registers), warps 6-9 copy and rescale this CTA's state rows (writing the
+// hi/lo copy into both CTAs' shared memory), warps 10-11 scale V.  Warp w reaches TMEM
+// lanes 32*(w%4)..+31.  Every wait is bounded;
 // a wait that gives up sets the device error word and both CTAs' abort flags, and the
 // CTAs unwind, meet at a final cluster barrier and free their tensor memory.
 //
@@ -42,9 +42,9 @@
 // Shared memory per CTA (1024-aligned, 224 KB), each box 128 rows x 64 bf16, 128B swizzle:
 //   Q   64 KB  own 128 query rows x 4 dk boxes
 //   K   64 KB  own 128 keys x 4 dk boxes (S); after S the K^T operand of the state update:
-//              all 256 keys x own 128 dk columns (2 dk boxes x 2 key blocks)
-//   V   32 KB  256 keys x own 64 value columns (scaled in place to Vz); once P.Vz has
-//              completed, the staging area of the output tiles (TMA stores)
+//              all 256 keys x own 128 dk columns (2 key blocks x 2 dk boxes; the own key
+//              block's boxes stay from S, the peer key block is loaded)
+//   V   32 KB  256 keys x own 64 value columns (scaled in place to Vz)
 //   Rhi 32 KB, Rlo 32 KB  bf16 copy of R_{i-1}: 256 dk rows x own 64 columns
 // MMA order in a chunk: S, Q.R, K^T.Vz, P.Vz; the K area is reloaded with the K^T operand
 // during Q.R and with the next chunk's keys during P.Vz.
@@ -59,7 +59,7 @@ __device__ unsigned g_err_chunkwise_pair;
 
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kB = 256;                        // chunk length
 constexpr int kDk = 256;
 constexpr int kBox = 128 * 128;                // 128 rows x 64 bf16
@@ -71,8 +71,8 @@ constexpr int kRloOff = kRhiOff + 2 * kBox;
 constexpr int kSmemBytes = kRloOff + 2 * kBox;  // 229376
 constexpr uint32_t kTS = 0, kTO = 256, kTR = 384;
 constexpr uint32_t kPairArrivals = 8;          // 4 warps in each CTA
+constexpr uint32_t kVArrivals = 4;             // the 2 V warps of each CTA
 constexpr uint16_t kBoth = 3;                  // multicast mask: both CTAs of the pair
-constexpr int kStoreWarp = 2;                  // its lane 0 issues the output TMA stores
 
 struct Decay {
     float l2g[kMaxHeads];   // log2(gamma)
@@ -83,13 +83,11 @@ struct Decay {
 struct Bars {
     // the even CTA's copies count both CTAs' work
     uint64_t q_full, k_full, kt_full;              // pair loads (transaction bytes)
-    uint64_t vz_ready, p_ready, rcopy, o_free;     // 8 warp arrivals
+    uint64_t vz_ready, p_ready, rcopy, o_free;     // warp arrivals of both CTAs
     // each CTA's own copy, arrived on by the MMA commits (multicast)
-    uint64_t q_empty, k_empty, kt_empty;
+    uint64_t q_empty, k_empty, kt_empty, v_empty;
     uint64_t s_full, o_full, r_done;
     uint64_t v_full;                               // local V load
-    uint64_t stage_written, stage_read;            // output staging rounds in the V area
-    uint64_t stage_free;                           // a chunk's output has left the V area
     uint64_t drain;
 };
 
@@ -104,11 +102,31 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
 }
 
+// Transpose the 8 x 8 grid of 16-byte items held by each group of 8 lanes: on return,
+// lane p of the group holds in a[k] the item p that lane k of the group held in a[p]
+// (three butterfly stages over lane bits 0-2).
+__device__ __forceinline__ void transpose8x8(uint32_t (&a)[8][4], int p8) {
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        const bool up = (p8 & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k & m) continue;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t x = __shfl_xor_sync(0xffffffffu, up ? a[k][w] : a[k | m][w], m);
+                if (up) a[k][w] = x; else a[k | m][w] = x;
+            }
+        }
+    }
+}
+
 template <bool OUT_BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                      const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
-                      const float* __restrict__ state_in, float* __restrict__ state_out, int N,
+                      const __grid_constant__ CUtensorMap mv,
+                      void* __restrict__ out_base, const float* __restrict__ state_in,
+                      float* __restrict__ state_out, int N,
                       int H, int dv, const Decay dc) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -129,20 +147,17 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
     const int bh = pair / nblk, blk = pair % nblk;
     const int head = bh % H;
     const int nchunks = N / kB;
-    constexpr int kOutRounds = OUT_BF16 ? 1 : 2;   // 32 KB staging rounds per 128 output columns
     volatile int* abort_p = &abort_flag;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full, 1); mbar_init(&bars.kt_full, 1);
-        mbar_init(&bars.vz_ready, kPairArrivals); mbar_init(&bars.p_ready, kPairArrivals);
+        mbar_init(&bars.vz_ready, kVArrivals); mbar_init(&bars.p_ready, kPairArrivals);
         mbar_init(&bars.rcopy, kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
         mbar_init(&bars.q_empty, 1); mbar_init(&bars.k_empty, 1);
-        mbar_init(&bars.kt_empty, 1);
+        mbar_init(&bars.kt_empty, 1); mbar_init(&bars.v_empty, 1);
         mbar_init(&bars.s_full, 1); mbar_init(&bars.o_full, 1); mbar_init(&bars.r_done, 1);
         mbar_init(&bars.v_full, 1); mbar_init(&bars.drain, 1);
-        mbar_init(&bars.stage_written, 4); mbar_init(&bars.stage_read, 1);
-        mbar_init(&bars.stage_free, 1);
         fence_barrier_init();
     }
     if (warp == 1) { tmem_alloc_pair(&tmem_slot, 512); tmem_relinquish_pair(); }
@@ -162,7 +177,6 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv);
-            tma_prefetch_desc(&mo);
             const uint32_t qf = lead(&bars.q_full), kf = lead(&bars.k_full), ktf = lead(&bars.kt_full);
             const int rowbase = bh * N;
             const int own = 128 * (int)rank, other = 128 * (int)peer;
@@ -196,21 +210,20 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (c > 0 && !w(&bars.kt_empty, (c - 1) & 1)) break;
                 if (rank == 0) { mbar_arrive_expect_tx(&bars.k_full, 2 * 4 * kBox); ++armed_k; }
                 for (int a = 0; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf);
-                // V: all keys of the chunk, own 64 value columns, once the previous chunk's
-                // output tiles have left the V area (one completion per chunk: a parity wait
-                // never runs more than one phase behind)
-                if (c > 0 && !w(&bars.stage_free, (uint32_t)(c - 1) & 1u)) break;
+                // V: all keys of the chunk, own 64 value columns (after the previous P.Vz)
+                if (c > 0 && !w(&bars.v_empty, (c - 1) & 1)) break;
                 mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
                 for (int j = 0; j < 2; ++j) tma_load_2d(sv + j * kBox, &mv, vcol, r0 + 128 * j, &bars.v_full);
                 ++v_loads;
-                // K^T operand: all keys, own dk half; box (m, j) = dk box 2*rank+m of key
-                // block j, placed so that each dk box holds keys 0..255 in order
+                // K^T operand of the state update: all keys x own dk half, as key block j,
+                // dk box m at (2j + m) boxes.  The own key block's boxes of the own dk half
+                // already sit there (K boxes 2*rank+m); once S has read the other two boxes,
+                // the peer key block takes their place (the same offsets in both CTAs).
                 if (!w(&bars.k_empty, c & 1)) break;
-                if (rank == 0) { mbar_arrive_expect_tx(&bars.kt_full, 2 * 4 * kBox); ++armed_kt; }
+                if (rank == 0) { mbar_arrive_expect_tx(&bars.kt_full, 2 * 2 * kBox); ++armed_kt; }
                 for (int m = 0; m < 2; ++m)
-                    for (int j = 0; j < 2; ++j)
-                        tma_load_2d_pair(sk + (2 * m + j) * kBox, &mk, 64 * (2 * (int)rank + m),
-                                         r0 + 128 * j, ktf);
+                    tma_load_2d_pair(sk + (2 * (int)peer + m) * kBox, &mk, 64 * (2 * (int)rank + m),
+                                     r0 + other, ktf);
             }
             if (!ok) {
                 // let loads in flight land before the CTAs unwind
@@ -232,7 +245,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             // descriptors are linear in the start address: base descriptor + offset / 16
             const uint64_t dQ = sdesc_sw128(smem_u32(sq), 16, 1024);
             const uint64_t dK = sdesc_sw128(smem_u32(sk), 16, 1024);
-            const uint64_t dKT = sdesc_sw128(smem_u32(sk), 2 * kBox, 1024);  // dk boxes 32 KB apart
+            const uint64_t dKT = sdesc_sw128(smem_u32(sk), kBox, 1024);   // dk boxes 16 KB apart
             const uint64_t dV = sdesc_sw128(smem_u32(sv), 2 * kBox, 1024);
             const uint64_t dRhi = sdesc_sw128(smem_u32(rhi), 2 * kBox, 1024);
             const uint64_t dRlo = sdesc_sw128(smem_u32(rlo), 2 * kBox, 1024);
@@ -275,8 +288,9 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 tc_fence_after();
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
+                    const uint64_t ka = (uint64_t)(((t >> 3) * 2 * kBox + (t & 7) * 2048) >> 4);
                     const uint64_t off = (uint64_t)((t * 2048) >> 4);
-                    mma_pair(tmem + kTR, dKT + off, dV + off, id_r, 1);
+                    mma_pair(tmem + kTR, dKT + ka, dV + off, id_r, 1);
                 }
                 mma_commit_pair(&bars.kt_empty, kBoth);
                 mma_commit_pair(&bars.r_done, kBoth);
@@ -291,14 +305,46 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     mma_pair_ts(tmem + kTO, a_hi + 16, bd, id_p, 1);
                 }
                 mma_commit_pair(&bars.o_full, kBoth);
+                mma_commit_pair(&bars.v_empty, kBoth);
             }
             // every issued MMA completes before tensor memory is released
             mma_commit_pair(&bars.drain, 1);
             mbar_wait(&bars.drain, 0, nullptr, 200000000ull);
         }
+    } else if (warp >= 10) {
+        // ------------------------------------------------------------ V scaling (warps 10-11)
+        // V row kr of the chunk scaled by g^(B-1-kr) in place (shared memory only)
+        const int vt = (int)threadIdx.x - 320;
+        const float l2g = dc.l2g[head];
+        for (int c = 0; c < nchunks; ++c) {
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&bars.v_full, (uint32_t)c & 1u, abort_p));
+            if (!got) {
+                if (lane == 0) fail();
+                break;
+            }
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int kr = vt + 64 * i;
+                const float f = exp2f(l2g * (float)(kB - 1 - kr));
+                uint8_t* vrow = sv + kr * 128;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint4* pv = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
+                    uint4 u = *pv;
+                    uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wv[e] = pack_bf16(bf16_lo(wv[e]) * f, bf16_hi(wv[e]) * f);
+                    *pv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cl(lead(&bars.vz_ready));
+        }
     } else {
         // ------------------------------------------------------------ transform warps
-        const bool pwarp = warp < 6;                 // warps 2-5: scores; 6-9: state/V/out
+        const bool pwarp = warp < 6;                 // warps 2-5: scores + output; 6-9: state
         const int q4 = warp & 3;                     // TMEM lane quarter of this warp
         const int row = 32 * q4 + lane;              // TMEM lane
         const uint32_t lrow = (uint32_t)(32 * q4) << 16;
@@ -316,70 +362,54 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             __syncwarp();
             if (lane == 0) mbar_arrive_cl(lead(bar));
         };
-        // output rows of chunk c: xi_j * O, staged as 128-byte-swizzled boxes (128 rows x
-        // 128 bytes) in the V area, which P.Vz no longer reads once o_full completed, and
-        // written by TMA stores: two boxes per round, 128 columns in kOutRounds rounds
+        // output rows of chunk c: xi_j * O, straight from registers.  Each 128-byte row
+        // segment (32 fp32 or 64 bf16 columns = 8 items of 16 bytes) is transposed within
+        // 8-lane groups (8 consecutive rows), so that every store instruction writes four
+        // whole 128-byte segments.  The last TMEM read releases O for the next Q.R.
         auto do_out = [&](int c) {
             if (!wait(&bars.o_full, (uint32_t)c & 1u)) return;
             tc_fence_after();
             const float xi = exp2f(l2g * (float)(j + 1));
-            const int orow0 = bh * N + c * kB + 128 * (int)rank;
-            constexpr int kBoxCols = OUT_BF16 ? 64 : 32;
+            const int p8 = lane & 7;
+            const size_t row0 = (size_t)bh * N + (size_t)c * kB + (size_t)(j - p8);
+            constexpr int kSegs = OUT_BF16 ? 2 : 4;           // 128-byte segments per 128 columns
+            constexpr int kSegCols = OUT_BF16 ? 64 : 32;
 #pragma unroll 1
-            for (int rr = 0; rr < kOutRounds; ++rr) {
-                const uint32_t n = (uint32_t)(c * kOutRounds + rr);   // staging round
-                if (rr > 0 && !wait(&bars.stage_read, (n - 1) & 1u)) return;
-#pragma unroll 1
-                for (int bx = 0; bx < 2; ++bx) {
-                    const uint32_t col0 = (uint32_t)((2 * rr + bx) * kBoxCols);
-                    uint8_t* srow = sv + bx * kBox + row * 128;
-                    if (OUT_BF16) {
-                        float o[64];
-                        tmem_ld32(tmem + lrow + kTO + col0, o);
-                        tmem_ld32(tmem + lrow + kTO + col0 + 32, o + 32);
-                        tmem_wait_ld();
+            for (int sg = 0; sg < kSegs; ++sg) {
+                uint32_t a[8][4];
+                if (OUT_BF16) {
+                    float o[64];
+                    tmem_ld32(tmem + lrow + kTO + 64 * sg, o);
+                    tmem_ld32(tmem + lrow + kTO + 64 * sg + 32, o + 32);
+                    tmem_wait_ld();
+                    if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc)
-                            *reinterpret_cast<uint4*>(srow + (((uint32_t)cc ^ ((uint32_t)row & 7u)) << 4)) =
-                                make_uint4(pack_bf16(xi * o[8 * cc], xi * o[8 * cc + 1]),
-                                           pack_bf16(xi * o[8 * cc + 2], xi * o[8 * cc + 3]),
-                                           pack_bf16(xi * o[8 * cc + 4], xi * o[8 * cc + 5]),
-                                           pack_bf16(xi * o[8 * cc + 6], xi * o[8 * cc + 7]));
-                    } else {
-                        float o[32];
-                        tmem_ld32(tmem + lrow + kTO + col0, o);
-                        tmem_wait_ld();
+                    for (int k = 0; k < 8; ++k)
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc)
-                            *reinterpret_cast<float4*>(srow + (((uint32_t)cc ^ ((uint32_t)row & 7u)) << 4)) =
-                                make_float4(xi * o[4 * cc], xi * o[4 * cc + 1], xi * o[4 * cc + 2],
-                                            xi * o[4 * cc + 3]);
-                    }
+                        for (int w = 0; w < 4; ++w)
+                            a[k][w] = pack_bf16(xi * o[8 * k + 2 * w], xi * o[8 * k + 2 * w + 1]);
+                } else {
+                    float o[32];
+                    tmem_ld32(tmem + lrow + kTO + 32 * sg, o);
+                    tmem_wait_ld();
+                    if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
                 }
-                if (rr == kOutRounds - 1) {
-                    tc_fence_before();
-                    arrive_lead(&bars.o_free);       // O read out: the next Q.R may overwrite it
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.stage_written);
-                if (warp == kStoreWarp) {
-                    bool good = true;
-                    if (lane == 0) {
-                        good = mbar_wait(&bars.stage_written, n & 1u, abort_p);
-                        if (good) {
-                            for (int bx = 0; bx < 2; ++bx)
-                                tma_store_3d(&mo, blk * 128 + (2 * rr + bx) * kBoxCols, orow0, 0,
-                                             sv + bx * kBox);
-                            bulk_commit();
-                            bulk_wait_read0();
-                            mbar_arrive(&bars.stage_read);
-                            if (rr == kOutRounds - 1) mbar_arrive(&bars.stage_free);
-                        } else {
-                            fail();
-                        }
-                    }
-                    if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) { ok = false; return; }
+                transpose8x8(a, p8);
+                const size_t col = (size_t)blk * 128 + (size_t)kSegCols * sg;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint4* dst;
+                    if (OUT_BF16)
+                        dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
+                                                       (row0 + k) * dv + col) + p8;
+                    else
+                        dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) + (row0 + k) * dv +
+                                                       col) + p8;
+                    *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
                 }
             }
         };
@@ -437,13 +467,10 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 // this chunk's output once its last P.Vz completed
                 do_out(c);
             }
-            if (warp == kStoreWarp && lane == 0) bulk_wait0();   // output stores complete
         } else {
             const float gB = dc.gB[head];
-            const uint32_t hi_local = smem_u32(rhi) + (uint32_t)j * 128u;
-            const uint32_t lo_local = smem_u32(rlo) + (uint32_t)j * 128u;
-            const uint32_t hi_peer = map_peer(rhi, peer) + (uint32_t)j * 128u;
-            const uint32_t lo_peer = map_peer(rlo, peer) + (uint32_t)j * 128u;
+            const uint32_t hi_peer = map_peer(rhi, peer);      // the peer's copy areas
+            const uint32_t lo_peer = map_peer(rlo, peer);
             // state: hi/lo copy of R_{i-1} (this CTA's dk row j, all 128 columns; columns
             // 64r.. go to CTA r), then R <- g^B R in TMEM
             auto do_state = [&](int c) {
@@ -451,10 +478,10 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
                     tc_fence_after();
                 }
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
+                // 32 columns (TMEM group g) of this CTA's state rows: R_{i-1} (from state_in
+                // for the first chunk), and R <- g^B R written back
+                auto load_scale = [&](int g, float* x) {
                     const uint32_t tcol = tmem + lrow + kTR + 32 * g;
-                    float x[32];
                     if (c == 0) {
                         if (state_in) {
                             const float4* src = reinterpret_cast<const float4*>(
@@ -472,60 +499,66 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                         tmem_ld32(tcol, x);
                         tmem_wait_ld();
                     }
-                    const bool local = (uint32_t)(g >> 1) == rank;
-                    const uint32_t hb = local ? hi_local : hi_peer;
-                    const uint32_t lb = local ? lo_local : lo_peer;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t h[4], l[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], h[e], l[e]);
-                        const uint32_t chunk = (uint32_t)(4 * (g & 1) + cc);
-                        const uint32_t off = ((chunk ^ ((uint32_t)j & 7u)) << 4);
-                        if (local) {
-                            *reinterpret_cast<uint4*>(rhi + j * 128 + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                            *reinterpret_cast<uint4*>(rlo + j * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
-                        } else {
-                            st_cluster_v4(hb + off, h[0], h[1], h[2], h[3]);
-                            st_cluster_v4(lb + off, l[0], l[1], l[2], l[3]);
-                        }
-                    }
+                };
+                auto rescale_store = [&](int g, float* x) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[e] *= gB;
-                    tmem_st32(tcol, x);
+                    tmem_st32(tmem + lrow + kTR + 32 * g, x);
+                };
+                // the peer's 64 columns first: hi/lo 16-byte chunks k = 8 columns each
+                uint32_t h[8][4], l[8][4];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int g = 2 * (int)peer + half;
+                    float x[32];
+                    load_scale(g, x);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], h[4 * half + cc][e], l[4 * half + cc][e]);
+                    rescale_store(g, x);
+                }
+                // transpose the 8 x 8 chunks of each 8-lane group (8 consecutive rows), so that
+                // remote store k writes whole 128-byte rows: lane p then holds chunk p of row
+                // j0 + k in slot k (j0 = j - p)
+                const int p8 = lane & 7;
+                transpose8x8(h, p8);
+                transpose8x8(l, p8);
+                {
+                    const uint32_t j0 = (uint32_t)(j - p8);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = (j0 + k) * 128u + (((uint32_t)p8 ^ (uint32_t)k) << 4);
+                        st_cluster_v4(hi_peer + off, h[k][0], h[k][1], h[k][2], h[k][3]);
+                        st_cluster_v4(lo_peer + off, l[k][0], l[k][1], l[k][2], l[k][3]);
+                    }
+                }
+                // this CTA's own 64 columns
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int g = 2 * (int)rank + half;
+                    float x[32];
+                    load_scale(g, x);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t hh[4], ll[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], hh[e], ll[e]);
+                        const uint32_t off = (uint32_t)j * 128u +
+                                             ((((uint32_t)(4 * half + cc)) ^ ((uint32_t)j & 7u)) << 4);
+                        *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<uint4*>(rlo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                    }
+                    rescale_store(g, x);
                 }
                 tmem_wait_st();
                 fence_proxy_async_cluster();
                 tc_fence_before();
                 arrive_lead(&bars.rcopy);
             };
-            // V rows kr = row and 128 + row of the chunk, scaled by g^(B-1-kr)
-            auto do_v = [&](int c) {
-                if (!wait(&bars.v_full, (uint32_t)c & 1u)) return;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int kr = 128 * half + row;
-                    const float f = exp2f(l2g * (float)(kB - 1 - kr));
-                    uint8_t* vrow = sv + kr * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint4* p = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
-                        uint4 u = *p;
-                        uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            wv[e] = pack_bf16(bf16_lo(wv[e]) * f, bf16_hi(wv[e]) * f);
-                        *p = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    }
-                }
-                fence_proxy_async();
-                arrive_lead(&bars.vz_ready);
-            };
-            for (int c = 0; c < nchunks && ok; ++c) {
-                do_state(c);
-                do_v(c);
-            }
+            for (int c = 0; c < nchunks && ok; ++c) do_state(c);
             // ---- final state: this CTA's dk rows of R_{N/B-1}
             if (ok && state_out && nchunks > 0) {
                 if (wait(&bars.r_done, (uint32_t)(nchunks - 1) & 1u)) {
@@ -576,10 +609,9 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     }
     const long long rows = (long long)b * H * N;
     if (rows >= (1LL << 31)) return cudaErrorNotSupported;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map_bf16(&mq, q, rows, dk, 128) || !make_map_bf16(&mk, k, rows, dk, 128) ||
-        !make_map_bf16(&mv, v, rows, dv, 128) ||
-        !make_map_3d_128b(&mo, o, out_bf16 != 0, 1, rows, dv, 128))
+        !make_map_bf16(&mv, v, rows, dv, 128))
         return cudaErrorInvalidValue;
     const long long grid = 2LL * b * H * (dv / 128);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -587,7 +619,7 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     auto kern = out_bf16 ? chunkwise_pair_kernel<true> : chunkwise_pair_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, mo, state_in, state_out, N, H, dv, dc);
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv, dc);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
     return e;
