@@ -84,6 +84,7 @@ struct Bars {
     // the even CTA's copies count both CTAs' work
     uint64_t q_full, k_full, kt_full;              // pair loads (transaction bytes)
     uint64_t vz_ready, p_ready, rcopy, o_free;     // warp arrivals of both CTAs
+
     // each CTA's own copy, arrived on by the MMA commits (multicast)
     uint64_t q_empty, k_empty, kt_empty, v_empty;
     uint64_t s_full, o_full, r_done;
@@ -153,7 +154,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
         abort_flag = 0;
         mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full, 1); mbar_init(&bars.kt_full, 1);
         mbar_init(&bars.vz_ready, kVArrivals); mbar_init(&bars.p_ready, kPairArrivals);
-        mbar_init(&bars.rcopy, kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
+        mbar_init(&bars.rcopy, 2 * kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
         mbar_init(&bars.q_empty, 1); mbar_init(&bars.k_empty, 1);
         mbar_init(&bars.kt_empty, 1); mbar_init(&bars.v_empty, 1);
         mbar_init(&bars.s_full, 1); mbar_init(&bars.o_full, 1); mbar_init(&bars.r_done, 1);
@@ -200,7 +201,6 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             };
             prefetch(0);
             for (int c = 0; c < nchunks && ok; ++c) {
-                prefetch(c + 1);
                 const int r0 = rowbase + c * kB;
                 // Q: own query rows, all dk (after the previous chunk's Q.R)
                 if (c > 0 && !w(&bars.q_empty, (c - 1) & 1)) break;
@@ -210,6 +210,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (c > 0 && !w(&bars.kt_empty, (c - 1) & 1)) break;
                 if (rank == 0) { mbar_arrive_expect_tx(&bars.k_full, 2 * 4 * kBox); ++armed_k; }
                 for (int a = 0; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf);
+                prefetch(c + 1);
                 // V: all keys of the chunk, own 64 value columns (after the previous P.Vz)
                 if (c > 0 && !w(&bars.v_empty, (c - 1) & 1)) break;
                 mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
@@ -322,7 +323,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (lane == 0) fail();
                 break;
             }
-#pragma unroll 1
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int kr = vt + 64 * i;
                 const float f = exp2f(l2g * (float)(kB - 1 - kr));
@@ -413,6 +414,101 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 }
             }
         };
+        // State copy for chunk c: the hi/lo bf16 copy of R_{i-1} (this CTA's dk row j) and
+        // R <- g^B R in TMEM.  The 64 columns of the peer's block (remote half, warps 6-9)
+        // are transposed within 8-lane groups so that each remote store writes whole
+        // 128-byte rows of the peer's copy; the own 64 columns (warps 2-5) go to this CTA's
+        // copy.  R_{-1} comes from state_in (zero without it).
+        const float gB = dc.gB[head];
+        const uint32_t hi_peer = map_peer(rhi, peer);
+        const uint32_t lo_peer = map_peer(rlo, peer);
+        auto do_state = [&](int c, bool remote) {
+            if (c > 0) {
+                if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
+                tc_fence_after();
+            }
+            auto load = [&](int g, float* x) {
+                if (c == 0) {
+                    if (state_in) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            state_in + ((size_t)bh * kDk + j) * dv + blk * 128 + 32 * g);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 f = src[e];
+                            x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) x[e] = 0.f;
+                    }
+                } else {
+                    tmem_ld32(tmem + lrow + kTR + 32 * g, x);
+                    tmem_wait_ld();
+                }
+            };
+            auto rescale_store = [&](int g, float* x) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] *= gB;
+                tmem_st32(tmem + lrow + kTR + 32 * g, x);
+            };
+            if (remote) {
+                // both column groups in flight at once
+                const int g0 = 2 * (int)peer;
+                float x[64];
+                if (c == 0) {
+                    load(g0, x);
+                    load(g0 + 1, x + 32);
+                } else {
+                    tmem_ld32(tmem + lrow + kTR + 32 * g0, x);
+                    tmem_ld32(tmem + lrow + kTR + 32 * g0 + 32, x + 32);
+                    tmem_wait_ld();
+                }
+                uint32_t h[8][4], l[8][4];      // 16-byte chunks k = 8 columns each
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1], h[k][e], l[k][e]);
+                // the rescaled state goes back now (asynchronous until tcgen05.wait::st)
+                rescale_store(g0, x);
+                rescale_store(g0 + 1, x + 32);
+                // lane p of an 8-lane group then holds chunk p of row j0 + k in slot k
+                const int p8 = lane & 7;
+                const uint32_t j0 = (uint32_t)(j - p8);
+                transpose8x8(h, p8);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_cluster_v4(hi_peer + (j0 + k) * 128u + (((uint32_t)p8 ^ (uint32_t)k) << 4), h[k][0],
+                                  h[k][1], h[k][2], h[k][3]);
+                transpose8x8(l, p8);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_cluster_v4(lo_peer + (j0 + k) * 128u + (((uint32_t)p8 ^ (uint32_t)k) << 4), l[k][0],
+                                  l[k][1], l[k][2], l[k][3]);
+            } else {
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int g = 2 * (int)rank + half;
+                    float x[32];
+                    load(g, x);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t hh[4], ll[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], hh[e], ll[e]);
+                        const uint32_t off = (uint32_t)j * 128u +
+                                             ((((uint32_t)(4 * half + cc)) ^ ((uint32_t)j & 7u)) << 4);
+                        *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<uint4*>(rlo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                    }
+                    rescale_store(g, x);
+                }
+            }
+            tmem_wait_st();
+            if (remote) fence_proxy_async_cluster(); else fence_proxy_async();
+            tc_fence_before();
+            arrive_lead(&bars.rcopy);
+        };
         if (pwarp) {
             const float cP = dc.cP[head];
             // P = g^(-B) S with the causal mask (key > j is zero), as hi/lo bf16 pairs in place.
@@ -433,6 +529,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     }
                 }
             };
+            if (nchunks > 0) do_state(0, false);
             for (int c = 0; c < nchunks && ok; ++c) {
                 if (!wait(&bars.s_full, (uint32_t)c & 1u)) break;
                 tc_fence_after();
@@ -464,101 +561,13 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 tmem_wait_st();
                 tc_fence_before();
                 arrive_lead(&bars.p_ready);
-                // this chunk's output once its last P.Vz completed
+                // while this chunk's last MMAs run: the own half of the next state copy
+                // (after K^T.Vz), then this chunk's output (after P.Vz)
+                if (c + 1 < nchunks) do_state(c + 1, false);
                 do_out(c);
             }
         } else {
-            const float gB = dc.gB[head];
-            const uint32_t hi_peer = map_peer(rhi, peer);      // the peer's copy areas
-            const uint32_t lo_peer = map_peer(rlo, peer);
-            // state: hi/lo copy of R_{i-1} (this CTA's dk row j, all 128 columns; columns
-            // 64r.. go to CTA r), then R <- g^B R in TMEM
-            auto do_state = [&](int c) {
-                if (c > 0) {
-                    if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
-                    tc_fence_after();
-                }
-                // 32 columns (TMEM group g) of this CTA's state rows: R_{i-1} (from state_in
-                // for the first chunk), and R <- g^B R written back
-                auto load_scale = [&](int g, float* x) {
-                    const uint32_t tcol = tmem + lrow + kTR + 32 * g;
-                    if (c == 0) {
-                        if (state_in) {
-                            const float4* src = reinterpret_cast<const float4*>(
-                                state_in + ((size_t)bh * kDk + j) * dv + blk * 128 + 32 * g);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float4 f = src[e];
-                                x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) x[e] = 0.f;
-                        }
-                    } else {
-                        tmem_ld32(tcol, x);
-                        tmem_wait_ld();
-                    }
-                };
-                auto rescale_store = [&](int g, float* x) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] *= gB;
-                    tmem_st32(tmem + lrow + kTR + 32 * g, x);
-                };
-                // the peer's 64 columns first: hi/lo 16-byte chunks k = 8 columns each
-                uint32_t h[8][4], l[8][4];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int g = 2 * (int)peer + half;
-                    float x[32];
-                    load_scale(g, x);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], h[4 * half + cc][e], l[4 * half + cc][e]);
-                    rescale_store(g, x);
-                }
-                // transpose the 8 x 8 chunks of each 8-lane group (8 consecutive rows), so that
-                // remote store k writes whole 128-byte rows: lane p then holds chunk p of row
-                // j0 + k in slot k (j0 = j - p)
-                const int p8 = lane & 7;
-                transpose8x8(h, p8);
-                transpose8x8(l, p8);
-                {
-                    const uint32_t j0 = (uint32_t)(j - p8);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (j0 + k) * 128u + (((uint32_t)p8 ^ (uint32_t)k) << 4);
-                        st_cluster_v4(hi_peer + off, h[k][0], h[k][1], h[k][2], h[k][3]);
-                        st_cluster_v4(lo_peer + off, l[k][0], l[k][1], l[k][2], l[k][3]);
-                    }
-                }
-                // this CTA's own 64 columns
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    const int g = 2 * (int)rank + half;
-                    float x[32];
-                    load_scale(g, x);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t hh[4], ll[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], hh[e], ll[e]);
-                        const uint32_t off = (uint32_t)j * 128u +
-                                             ((((uint32_t)(4 * half + cc)) ^ ((uint32_t)j & 7u)) << 4);
-                        *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                        *reinterpret_cast<uint4*>(rlo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-                    }
-                    rescale_store(g, x);
-                }
-                tmem_wait_st();
-                fence_proxy_async_cluster();
-                tc_fence_before();
-                arrive_lead(&bars.rcopy);
-            };
-            for (int c = 0; c < nchunks && ok; ++c) do_state(c);
+            for (int c = 0; c < nchunks && ok; ++c) do_state(c, true);
             // ---- final state: this CTA's dk rows of R_{N/B-1}
             if (ok && state_out && nchunks > 0) {
                 if (wait(&bars.r_done, (uint32_t)(nchunks - 1) & 1u)) {
