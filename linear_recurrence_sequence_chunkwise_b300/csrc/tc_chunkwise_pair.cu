@@ -210,7 +210,6 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (c > 0 && !w(&bars.kt_empty, (c - 1) & 1)) break;
                 if (rank == 0) { mbar_arrive_expect_tx(&bars.k_full, 2 * 4 * kBox); ++armed_k; }
                 for (int a = 0; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf);
-                prefetch(c + 1);
                 // V: all keys of the chunk, own 64 value columns (after the previous P.Vz)
                 if (c > 0 && !w(&bars.v_empty, (c - 1) & 1)) break;
                 mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
@@ -225,6 +224,8 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 for (int m = 0; m < 2; ++m)
                     tma_load_2d_pair(sk + (2 * (int)peer + m) * kBox, &mk, 64 * (2 * (int)rank + m),
                                      r0 + other, ktf);
+                // the next chunk's boxes into L2, behind this chunk's loads in the TMA queue
+                prefetch(c + 1);
             }
             if (!ok) {
                 // let loads in flight land before the CTAs unwind
