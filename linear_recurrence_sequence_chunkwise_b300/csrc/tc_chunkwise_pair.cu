@@ -103,25 +103,6 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
 }
 
-// Transpose the 8 x 8 grid of 16-byte items held by each group of 8 lanes: on return,
-// lane p of the group holds in a[k] the item p that lane k of the group held in a[p]
-// (three butterfly stages over lane bits 0-2).
-__device__ __forceinline__ void transpose8x8(uint32_t (&a)[8][4], int p8) {
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
-        const bool up = (p8 & m) != 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k & m) continue;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t x = __shfl_xor_sync(0xffffffffu, up ? a[k][w] : a[k | m][w], m);
-                if (up) a[k][w] = x; else a[k | m][w] = x;
-            }
-        }
-    }
-}
-
 template <bool OUT_BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,

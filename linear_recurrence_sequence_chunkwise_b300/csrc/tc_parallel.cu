@@ -40,6 +40,7 @@
 // write the outputs (group g takes half of the value columns).  Every wait is
 // bounded; a wait that gives up sets the device error word and the CTA unwinds.
 //
+// Outputs leave from registers as coalesced 128-byte row segments (8-lane transposes).
 // Tensor memory (512 columns): [0,256) O (W fp32 columns), [256,384) and [384,512) S.
 // Shared memory: Q (dk/128 pieces) + 5 ring pieces = 224 KB at dk = 256.
 #include "common.cuh"
@@ -70,6 +71,7 @@ struct ParConsts {
 // Fused gated epilogue ([RN2] "門控多尺度 Retention"): GroupNorm over the dv outputs of
 // each (token, head), optional per-channel affine, times swish(G).
 struct EpiArgs {
+    void* out;              // the output: [b][H][N][dv] (EPI = 0) or [b][N][H*dv]
     const void* g;          // [b][N][H*dv], fp32 or bf16 (template EPI); read through a TMA map
     const float* weight;    // [H*dv] or NULL
     const float* bias;      // [H*dv] or NULL
@@ -168,7 +170,6 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv);
-            tma_prefetch_desc(&mo);
             if (EPI != 0) tma_prefetch_desc(&mg);
             mbar_arrive_expect_tx(&bars.q_full, NH * kPiece);
             for (int hh = 0; hh < NH; ++hh)
@@ -418,11 +419,13 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         __syncwarp();
         cluster_sync_all();
     }
-    // ---- staged output: per transform group, 64-column chunks of the group's W/2 columns.
-    // The ring is free once o_full has completed; each group uses 64 KB of it: a gate
-    // tile (TMA load) and an output tile (written here, stored by TMA, rows past N are
-    // clipped by the store).  Both tiles use the 128-byte swizzle: the 16-byte chunk c of
-    // row r sits at chunk position c ^ (r % 8) of a 128-row x 128-byte atom.
+    // ---- output: per transform group, 64-column chunks of the group's W/2 columns, stored
+    // from registers.  Each 128-byte row segment (32 fp32 or 64 bf16 values = 8 items of
+    // 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so that every
+    // store instruction writes four whole 128-byte segments; rows past N are skipped.
+    // Without the gate prefetch, the ring (free once o_full has completed) takes a gate
+    // tile per chunk (TMA load, 128-byte swizzle: the 16-byte chunk c of row r sits at
+    // chunk position c ^ (r % 8) of a 128-row x 128-byte atom).
     if (warp >= 2) {
         const int grp = (warp - 2) >> 2;
         const int q4 = warp & 3;
@@ -432,9 +435,7 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const bool issuer = (threadIdx.x == (unsigned)(64 + 128 * grp));   // lane 0 of warp 2 / 6
         constexpr int kCols = W / 2;
         constexpr int kChunks = kEpiChunks;
-        constexpr int kOutAtoms = OUT_BF16 ? 1 : 2;
         constexpr int kGAtoms = (EPI == 2) ? 1 : 2;
-        uint8_t* ost = ring + 8192 + grp * 65536 + 32768;  // output staging (up to 2 atoms)
         const float inv = row_inv;
         float mean = 0.f, rstd = 1.f;
         if (EPI != 0) {
@@ -451,89 +452,101 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const bool live = __all_sync(0xffffffffu, abort_flag == 0);
         if (live) tc_fence_after();
         auto swz = [&](int c16) { return (uint32_t)(row * 128 + ((((uint32_t)c16) ^ (row & 7)) << 4)); };
+        const int p8 = lane & 7;
+        const int r0 = row - p8;                                     // first row of the 8-lane group
+        const size_t row_elems = (EPI != 0) ? (size_t)H * dv : (size_t)dv;
+        const size_t row_base = (EPI != 0) ? (size_t)bi * N : (size_t)bh * N;
 #pragma unroll 1
         for (int ch = 0; ch < kChunks; ++ch) {
             const int col = W * vb + kCols * grp + 64 * ch;          // first value column
-            const int gcol = (EPI != 0) ? head * dv + col : col;     // column in the global map
+            const int gcol = (EPI != 0) ? head * dv + col : col;     // column in the output row
             const int plane = (EPI != 0) ? bi : bh;
             uint8_t* gst = kGPrefetch ? qarea + (grp * kEpiChunks + ch) * 16384   // gate tile
                                       : ring + 8192 + grp * 65536;
-            if (issuer) {
-                bulk_wait_read0();                                   // staging free again
-                if (EPI != 0 && !kGPrefetch && live) {
-                    mbar_arrive_expect_tx(&bars.g_full[grp], kGAtoms * 16384);
-                    for (int a2 = 0; a2 < kGAtoms; ++a2)
-                        tma_load_3d(gst + a2 * 16384, &mg, gcol + a2 * (EPI == 2 ? 64 : 32), n0, plane,
-                                    &bars.g_full[grp]);
-                }
+            if (issuer && EPI != 0 && !kGPrefetch && live) {
+                mbar_arrive_expect_tx(&bars.g_full[grp], kGAtoms * 16384);
+                for (int a2 = 0; a2 < kGAtoms; ++a2)
+                    tma_load_3d(gst + a2 * 16384, &mg, gcol + a2 * (EPI == 2 ? 64 : 32), n0, plane,
+                                &bars.g_full[grp]);
             }
-            named_bar(6 + grp, 128);
             bool got_g = true;
             if (EPI != 0 && live) {
                 got_g = kGPrefetch ? __all_sync(0xffffffffu, mbar_wait(&bars.g_pre, 0, abort_p))
                                    : __all_sync(0xffffffffu, mbar_wait(&bars.g_full[grp], ch & 1, abort_p));
             }
             if (live && got_g) {
-                float o[64];
-                tmem_ld32(tmem + lrow + kTO + kCols * grp + 64 * ch, o);
-                tmem_ld32(tmem + lrow + kTO + kCols * grp + 64 * ch + 32, o + 32);
-                float gv[64];
-                if (EPI == 2) {
+                uint32_t a[8][4];                                    // bf16: the chunk's 8 items
 #pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(gst + swz(c16));
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                for (int hf = 0; hf < 2; ++hf) {                     // 32-column halves
+                    float o[32];
+                    tmem_ld32(tmem + lrow + kTO + kCols * grp + 64 * ch + 32 * hf, o);
+                    float gv[32];
+                    if (EPI == 2) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            gv[8 * c16 + 2 * e] = __uint_as_float(w4[e] << 16);
-                            gv[8 * c16 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(gst + swz(4 * hf + c));
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                gv[8 * c + 2 * e] = __uint_as_float(w4[e] << 16);
+                                gv[8 * c + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                            }
+                        }
+                    } else if (EPI == 1) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 f = *reinterpret_cast<const float4*>(gst + hf * 16384 + swz(c));
+                            gv[4 * c] = f.x; gv[4 * c + 1] = f.y; gv[4 * c + 2] = f.z; gv[4 * c + 3] = f.w;
                         }
                     }
-                } else if (EPI == 1) {
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int c16 = 0; c16 < 16; ++c16) {
-                        const float4 f = *reinterpret_cast<const float4*>(gst + (c16 / 8) * 16384 + swz(c16 % 8));
-                        gv[4 * c16] = f.x; gv[4 * c16 + 1] = f.y; gv[4 * c16 + 2] = f.z; gv[4 * c16 + 3] = f.w;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        if (EPI == 0) {
+                            o[jj] = o[jj] * inv;
+                        } else {
+                            float yn = (o[jj] * inv - mean) * rstd;
+                            const int ch_ = head * dv + col + 32 * hf + jj;
+                            if (ea.weight) yn *= ea.weight[ch_];
+                            if (ea.bias) yn += ea.bias[ch_];
+                            // swish with the hardware exp2/reciprocal paths (a few ulp, far
+                            // inside the bf16-input tolerance); g -> -inf gives g * 0 = -0
+                            o[jj] = __fdividef(gv[jj], 1.0f + __expf(-gv[jj])) * yn;
+                        }
                     }
-                }
-                tmem_wait_ld();
-                float* r = o;                                        // results replace O in place
+                    if (OUT_BF16) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    if (EPI == 0) {
-                        r[j] = o[j] * inv;
+                        for (int k = 0; k < 4; ++k)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                a[4 * hf + k][w] = pack_bf16(o[8 * k + 2 * w], o[8 * k + 2 * w + 1]);
                     } else {
-                        float yn = (o[j] * inv - mean) * rstd;
-                        const int ch_ = head * dv + col + j;
-                        if (ea.weight) yn *= ea.weight[ch_];
-                        if (ea.bias) yn += ea.bias[ch_];
-                        // swish with the hardware exp2/reciprocal paths (a few ulp, far inside
-                        // the bf16-input tolerance); g -> -inf gives g * 0 = -0
-                        r[j] = __fdividef(gv[j], 1.0f + __expf(-gv[j])) * yn;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(o[4 * k + w]);
+                    }
+                    if (!OUT_BF16 || hf == 1) {
+                        // one 128-byte segment: 32 fp32 (this half) or 64 bf16 (the chunk)
+                        transpose8x8(a, p8);
+                        const int c0 = gcol + (OUT_BF16 ? 0 : 32 * hf);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int n_out = n0 + r0 + k;
+                            if (n_out < N) {
+                                const size_t e0 = (row_base + (size_t)n_out) * row_elems + (size_t)c0;
+                                uint4* dst = OUT_BF16
+                                    ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ea.out) + e0) + p8
+                                    : reinterpret_cast<uint4*>(static_cast<float*>(ea.out) + e0) + p8;
+                                *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
+                            }
+                        }
                     }
                 }
-                if (OUT_BF16) {
-#pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16)
-                        *reinterpret_cast<uint4*>(ost + swz(c16)) =
-                            make_uint4(pack_bf16(r[8 * c16], r[8 * c16 + 1]), pack_bf16(r[8 * c16 + 2], r[8 * c16 + 3]),
-                                       pack_bf16(r[8 * c16 + 4], r[8 * c16 + 5]), pack_bf16(r[8 * c16 + 6], r[8 * c16 + 7]));
-                } else {
-#pragma unroll
-                    for (int c16 = 0; c16 < 16; ++c16)
-                        *reinterpret_cast<float4*>(ost + (c16 / 8) * 16384 + swz(c16 % 8)) =
-                            make_float4(r[4 * c16], r[4 * c16 + 1], r[4 * c16 + 2], r[4 * c16 + 3]);
-                }
             }
-            fence_proxy_async();
-            named_bar(6 + grp, 128);
-            if (issuer && live && got_g) {
-                for (int a2 = 0; a2 < kOutAtoms; ++a2)
-                    tma_store_3d(&mo, gcol + a2 * (OUT_BF16 ? 64 : 32), n0, plane, ost + a2 * 16384);
-                bulk_commit();
-            }
+            // every warp of the group is done with this chunk's gate tile
+            if (!kGPrefetch && EPI != 0) named_bar(6 + grp, 128);
         }
-        if (issuer) bulk_wait0();
     }
     __syncwarp();
     tc_fence_before();
@@ -631,7 +644,9 @@ cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, 
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o, int out_bf16,
                                int b, int H, int N, int dk, int dv, const HeadConsts& hc,
                                unsigned flags, cudaStream_t s) {
-    return launch_common(q, k, v, o, out_bf16, b, H, N, dk, dv, hc, flags, 0, EpiArgs{}, s);
+    EpiArgs ea{};
+    ea.out = o;
+    return launch_common(q, k, v, o, out_bf16, b, H, N, dk, dv, hc, flags, 0, ea, s);
 }
 
 cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v, const void* g,
@@ -640,6 +655,7 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
                                      float eps, const float* weight, const float* bias,
                                      cudaStream_t s) {
     EpiArgs ea;
+    ea.out = out;
     ea.g = g;
     ea.weight = weight;
     ea.bias = bias;
