@@ -24,13 +24,12 @@
 // pairs instead of dv/64 CTAs.  The pair costs one duplicated quarter of the score tile
 // (the even CTA's rows against keys 128-255, all masked) and of P.V.
 //
-// Roles (384 threads per CTA): warp 0 issues this CTA's TMA loads (Q, K and the K^T
+// Roles (320 threads per CTA): warp 0 issues this CTA's TMA loads (Q, K and the K^T
 // operand complete on the even CTA's barriers, V on a local one), warp 1 allocates
 // tensor memory (both CTAs, collectively) and, in the even CTA, issues the MMAs, warps
 // 2-5 turn this CTA's score rows into P and then write its output rows (coalesced stores
-// from registers), warps 6-9 copy and rescale this CTA's state rows (writing the
-// hi/lo copy into both CTAs' shared memory), warps 10-11 scale V.  Warp w reaches TMEM
-// lanes 32*(w%4)..+31.  Every wait is bounded;
+// from registers), warps 6-9 copy the peer half of this CTA's state rows (into the
+// peer's shared memory) and scale V.  Warp w reaches TMEM lanes 32*(w%4)..+31.  Every wait is bounded;
 // a wait that gives up sets the device error word and both CTAs' abort flags, and the
 // CTAs unwind, meet at a final cluster barrier and free their tensor memory.
 //
@@ -59,7 +58,7 @@ __device__ unsigned g_err_chunkwise_pair;
 
 using namespace tc;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;
 constexpr int kB = 256;                        // chunk length
 constexpr int kDk = 256;
 constexpr int kBox = 128 * 128;                // 128 rows x 64 bf16
@@ -71,7 +70,6 @@ constexpr int kRloOff = kRhiOff + 2 * kBox;
 constexpr int kSmemBytes = kRloOff + 2 * kBox;  // 229376
 constexpr uint32_t kTS = 0, kTO = 256, kTR = 384;
 constexpr uint32_t kPairArrivals = 8;          // 4 warps in each CTA
-constexpr uint32_t kVArrivals = 4;             // the 2 V warps of each CTA
 constexpr uint16_t kBoth = 3;                  // multicast mask: both CTAs of the pair
 
 struct Decay {
@@ -134,7 +132,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full, 1); mbar_init(&bars.kt_full, 1);
-        mbar_init(&bars.vz_ready, kVArrivals); mbar_init(&bars.p_ready, kPairArrivals);
+        mbar_init(&bars.vz_ready, kPairArrivals); mbar_init(&bars.p_ready, kPairArrivals);
         mbar_init(&bars.rcopy, 2 * kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
         mbar_init(&bars.q_empty, 1); mbar_init(&bars.k_empty, 1);
         mbar_init(&bars.kt_empty, 1); mbar_init(&bars.v_empty, 1);
@@ -293,37 +291,6 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             // every issued MMA completes before tensor memory is released
             mma_commit_pair(&bars.drain, 1);
             mbar_wait(&bars.drain, 0, nullptr, 200000000ull);
-        }
-    } else if (warp >= 10) {
-        // ------------------------------------------------------------ V scaling (warps 10-11)
-        // V row kr of the chunk scaled by g^(B-1-kr) in place (shared memory only)
-        const int vt = (int)threadIdx.x - 320;
-        const float l2g = dc.l2g[head];
-        for (int c = 0; c < nchunks; ++c) {
-            const bool got = __all_sync(0xffffffffu, mbar_wait(&bars.v_full, (uint32_t)c & 1u, abort_p));
-            if (!got) {
-                if (lane == 0) fail();
-                break;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int kr = vt + 64 * i;
-                const float f = exp2f(l2g * (float)(kB - 1 - kr));
-                uint8_t* vrow = sv + kr * 128;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint4* pv = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
-                    uint4 u = *pv;
-                    uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        wv[e] = pack_bf16(bf16_lo(wv[e]) * f, bf16_hi(wv[e]) * f);
-                    *pv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cl(lead(&bars.vz_ready));
         }
     } else {
         // ------------------------------------------------------------ transform warps
@@ -549,7 +516,32 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 do_out(c);
             }
         } else {
-            for (int c = 0; c < nchunks && ok; ++c) do_state(c, true);
+            // V rows kr = row and 128 + row of chunk c scaled in place by g^(B-1-kr); the
+            // block lands after the previous P.Vz, while this group copies the state
+            auto do_v = [&](int c) {
+                if (!wait(&bars.v_full, (uint32_t)c & 1u)) return;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int kr = 128 * half + row;
+                    const float f = exp2f(l2g * (float)(kB - 1 - kr));
+                    uint8_t* vrow = sv + kr * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint4* pv = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
+                        uint4 u = *pv;
+                        uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) wv[e] = pack_bf16(bf16_lo(wv[e]) * f, bf16_hi(wv[e]) * f);
+                        *pv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+                fence_proxy_async();
+                arrive_lead(&bars.vz_ready);
+            };
+            for (int c = 0; c < nchunks && ok; ++c) {
+                do_state(c, true);
+                do_v(c);
+            }
             // ---- final state: this CTA's dk rows of R_{N/B-1}
             if (ok && state_out && nchunks > 0) {
                 if (wait(&bars.r_done, (uint32_t)(nchunks - 1) & 1u)) {
