@@ -137,3 +137,20 @@ def test_tc_chunkwise_repeatable_and_guarded(chunk, dv):
     assert torch.equal(first, o)
     assert guards_intact(buf)
     assert err_bf16(o, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
+
+
+@pytest.mark.parametrize("b,H,N,dv", [(3, 5, 256, 256), (1, 1, 512, 384), (2, 3, 768, 128)])
+def test_tc_chunkwise_pair_edges(b, H, N, dv):
+    """The pair kernel with one 256-token chunk, odd batch and head counts, one to three
+    128-column value blocks, and an incoming state carried to the final state."""
+    dk, chunk = 256, 256
+    q, k, v = mk(b, H, N, dk, dv, 900 + N + dv + H)
+    g = inputs.gammas(H)
+    s0 = inputs.randn((b, H, dk, dv), 901 + N, 0.05, "f32", DEV)
+    st = s0.clone()
+    got = rb.retention_chunkwise(q, k, v, g, chunk, state_in=st, state_out=st)
+    assert rb.last_kernel() == "chunkwise_tc_pair"
+    want, s_end = oracle.chunkwise(q, k, v, g, chunk, state_in=s0.cpu(), return_state=True)
+    assert err_bf16(got, want) < TOL_BF16
+    assert err_f32(st, s_end) < TOL_BF16
+    rb.check_device_error()
