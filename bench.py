@@ -254,7 +254,6 @@ def workload_config(w, out_dtype: str):
 
 
 def bench_chunkwise(args, dist, rb, pk, out_dtype):
-    from linear_recurrence_sequence_chunkwise_b300 import streaming
     w = inputs.CHUNKWISE_LONG
     q, k, v = inputs.qkv(w, "cuda")
     od = torch.float32 if out_dtype == "f32" else torch.bfloat16
@@ -279,16 +278,18 @@ def bench_chunkwise(args, dist, rb, pk, out_dtype):
                         "algorithmic_flops_per_launch": flops,
                         "algorithmic_bytes_per_launch": in_bytes + out_bytes,
                         "achieved_gbs": (in_bytes + out_bytes) / (ms_step * 1e-3) / 1e9}}
-    # end to end through the public API with host buffers: every step copies q, k, v
-    # from pinned host memory and the output back.  The sequence streams through in
-    # segments whose state is carried exactly (eq.7), so the copies of one segment
-    # overlap the compute of the next on separate streams.
+    # end to end through the C ABI with host buffers (retention_chunkwise_host): every step
+    # copies q, k, v from pinned host memory and the output back; the sequence streams
+    # through in segments whose state is carried exactly (eq.7), so the copies of one
+    # segment overlap the compute of the next on separate streams.
     hq, hk, hv = (t.to("cpu").pin_memory() for t in (q, k, v))
     ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     seg = E2E_SEGMENT
+    ws = torch.empty(rb.chunkwise_host_workspace_bytes(q.dtype, o.dtype, w.b, w.H, w.dk, w.dv, seg),
+                     dtype=torch.uint8, device="cuda")
 
     def e2e_step():
-        streaming.chunkwise_from_host(hq, hk, hv, w.gamma, w.chunk, ho, seg)
+        rb.retention_chunkwise_host(hq, hk, hv, w.gamma, w.chunk, ho, seg, workspace=ws)
 
     e2e_steps = max(1, min(args.steps, 5))
     ms_e2e, _ = timed(e2e_step, e2e_steps, 1, dist)
@@ -296,8 +297,9 @@ def bench_chunkwise(args, dist, rb, pk, out_dtype):
     rb.check_device_error()
     res["e2e"] = {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": in_bytes,
                   "d2h_bytes_per_step": out_bytes, "ms_per_step": ms_e2e / e2e_steps,
-                  "mode": f"pinned host q/k/v/out, {w.N // seg} segments of {seg} tokens, "
-                          f"H2D / compute / D2H on three streams, state carried on device"}
+                  "mode": f"retention_chunkwise_host: pinned host q/k/v/out, {w.N // seg} segments "
+                          f"of {seg} tokens, H2D / compute / D2H on three streams, state carried "
+                          f"on the device"}
     del q, k, v, o, hq, hk, hv, ho
     torch.cuda.empty_cache()
     return res

@@ -42,6 +42,8 @@
 #ifndef RETENTION_B300_H
 #define RETENTION_B300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -94,6 +96,47 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
                         ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
                         int dk, int dv, int chunk, const double* gamma,
                         const float* state_in, float* state_out, void* stream);
+
+/*
+ * retention_chunkwise over HOST-resident inputs and outputs.  The sequence passes
+ * through the device in segments of seg_len tokens (a multiple of chunk dividing N);
+ * eq.(7) carries the state across any split at a chunk boundary ([RN2] "Retention" 3)),
+ * so each segment continues from the fp32 state the previous one left in the workspace
+ * and the result is that of one retention_chunkwise call over the whole sequence.
+ * Per segment: host-to-device copies of Q, K, V on h2d_stream (one 2-D copy each),
+ * the chunkwise call on stream, the device-to-host copy of O on d2h_stream; two
+ * buffer sets alternate, so one segment's copies overlap its neighbours' compute.
+ *
+ * q, k: [b][H][N][dk], v: [b][H][N][dv] (in_dtype), o: [b][H][N][dv] (out_dtype), all
+ * HOST pointers, 16-byte aligned; pinned (page-locked) memory makes the copies
+ * asynchronous.  state_in, state_out: DEVICE pointers [b][H][dk][dv] fp32, nullable,
+ * as in retention_chunkwise.  workspace: DEVICE memory of at least
+ * retention_chunkwise_host_workspace_bytes(...) bytes, 256-byte aligned, owned by the
+ * caller and not touched by anything else until stream reaches this call's end.
+ * h2d_stream, d2h_stream: two further streams (cudaStream_t) for the copies, distinct
+ * from stream and from each other for the copies to overlap.  The call returns once
+ * everything is enqueued; all of its work is ordered on stream (the copy streams first
+ * wait for the work queued on stream before the call, and stream waits for the last
+ * copy).  The library creates and releases a few CUDA events inside the call.
+ * Argument checks (those of retention_chunkwise, plus seg_len > 0 with seg_len % chunk
+ * == 0 and N % seg_len == 0, and the workspace size: RET_ERR_SHAPE) run before the
+ * first copy.  A CUDA error or a failed segment returns its status; earlier segments
+ * may then have been written.
+ */
+int retention_chunkwise_host(const void* q, const void* k, const void* v, void* o,
+                             ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                             int dk, int dv, int chunk, const double* gamma,
+                             const float* state_in, float* state_out, int seg_len,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* h2d_stream, void* d2h_stream);
+
+/*
+ * Bytes of device workspace retention_chunkwise_host needs for these dtypes and sizes
+ * (the carried state and two segment buffer sets); 0 for invalid dtypes or negative
+ * sizes.  Host-side, no GPU access.
+ */
+size_t retention_chunkwise_host_workspace_bytes(ret_dtype in_dtype, ret_dtype out_dtype, int b,
+                                                int H, int dk, int dv, int seg_len);
 
 /*
  * One decode step of the recurrent form, [RN2] "Retention" 2) eq.(6) and the

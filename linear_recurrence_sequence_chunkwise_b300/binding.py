@@ -62,6 +62,10 @@ def lib() -> ctypes.CDLL:
             L.msr_epilogue.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, vp]
             L.retention_parallel_gated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp,
                                                    u, f, vp, vp, vp]
+            L.retention_chunkwise_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp,
+                                                   vp, vp, i, vp, ctypes.c_size_t, vp, vp, vp]
+            L.retention_chunkwise_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+            L.retention_chunkwise_host_workspace_bytes.restype = ctypes.c_size_t
             L.retention_status_string.argtypes = [i]
             L.retention_status_string.restype = ctypes.c_char_p
             L.retention_check_device_error.argtypes = [vp]
@@ -75,7 +79,7 @@ def lib() -> ctypes.CDLL:
             L.retention_cuda_error_string.restype = ctypes.c_char_p
             for name in ("retention_parallel", "retention_chunkwise", "retention_recurrent_step",
                          "msr_epilogue", "retention_check_device_error",
-                         "retention_parallel_gated"):
+                         "retention_parallel_gated", "retention_chunkwise_host"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -158,6 +162,50 @@ def retention_chunkwise(q, k, v, gamma, chunk: int, state_in=None, state_out=Non
                                    _gamma(gamma, H), _ptr(state_in), _ptr(state_out),
                                    _stream(stream))
     _check("retention_chunkwise", rc)
+    return out
+
+
+_copy_streams = {}
+
+
+def _host_ptr(t):
+    if t.is_cuda:
+        raise ValueError("host tensors expected (pinned CPU memory)")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def chunkwise_host_workspace_bytes(in_dtype, out_dtype, b: int, H: int, dk: int, dv: int,
+                                   seg_len: int) -> int:
+    return int(lib().retention_chunkwise_host_workspace_bytes(
+        _dtype_code(in_dtype), _dtype_code(out_dtype), b, H, dk, dv, seg_len))
+
+
+def retention_chunkwise_host(q, k, v, gamma, chunk: int, out, seg_len: int, state_in=None,
+                             state_out=None, workspace=None, stream=None, copy_streams=None):
+    """Chunkwise form over host tensors (pinned CPU q,k:[b,H,N,dk] v,out:[b,H,N,dv]),
+    streamed through the device in segments of seg_len tokens.  Device workspace and the
+    two copy streams are made here unless given; all work is ordered on `stream`."""
+    b, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        nbytes = chunkwise_host_workspace_bytes(q.dtype, out.dtype, b, H, dk, dv, seg_len)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    if copy_streams is None:
+        if dev.index not in _copy_streams:
+            _copy_streams[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        copy_streams = _copy_streams[dev.index]
+    rc = lib().retention_chunkwise_host(
+        _host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(out), _dtype_code(q.dtype),
+        _dtype_code(out.dtype), b, H, N, dk, dv, chunk, _gamma(gamma, H), _ptr(state_in),
+        _ptr(state_out), seg_len, ctypes.c_void_p(workspace.data_ptr()),
+        ctypes.c_size_t(workspace.numel()), _stream(stream),
+        ctypes.c_void_p(copy_streams[0].cuda_stream), ctypes.c_void_p(copy_streams[1].cuda_stream))
+    _check("retention_chunkwise_host", rc)
     return out
 
 

@@ -103,6 +103,9 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
 // Count one successful kernel launch (host-side, process-wide) and record its
 // RET_KERNEL_* code for the launching host thread.
 void count_launch(int kernel_code);
+// RET_OK for cudaSuccess; otherwise records the error for retention_last_cuda_error and
+// returns RET_ERR_CUDA.
+int record_cuda_status(cudaError_t e);
 // Device error words of the kernels with bounded waits: read and clear.
 unsigned read_clear_error_tc_chunkwise(cudaStream_t s);
 unsigned read_clear_error_tc_chunkwise_pair(cudaStream_t s);

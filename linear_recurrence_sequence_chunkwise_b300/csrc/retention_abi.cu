@@ -21,6 +21,11 @@ void count_launch(int kernel_code) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     t_last_kernel = kernel_code;
 }
+int record_cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return RET_OK;
+    t_last_cuda_error = (int)e;
+    return RET_ERR_CUDA;
+}
 }  // namespace ret
 
 namespace {
@@ -50,11 +55,7 @@ int head_consts(const double* gamma, int H, int B, HeadConsts* hc) {
     return RET_OK;
 }
 
-int cuda_status(cudaError_t e) {
-    if (e == cudaSuccess) return RET_OK;
-    ret::t_last_cuda_error = (int)e;
-    return RET_ERR_CUDA;
-}
+int cuda_status(cudaError_t e) { return ret::record_cuda_status(e); }
 
 }  // namespace
 

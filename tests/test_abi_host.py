@@ -34,7 +34,8 @@ def test_exports_every_declared_function(L):
                           "msr_epilogue", "retention_status_string",
                           "retention_check_device_error", "retention_kernel_launches",
                           "retention_last_kernel", "retention_last_cuda_error",
-                          "retention_cuda_error_string", "retention_parallel_gated"}
+                          "retention_cuda_error_string", "retention_parallel_gated",
+                          "retention_chunkwise_host", "retention_chunkwise_host_workspace_bytes"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
@@ -177,3 +178,45 @@ def test_binding_refuses_cpu_tensors(L):
     q = torch.zeros(1, 1, 16, 16)
     with pytest.raises(ValueError):
         binding.retention_parallel(q, q, q, [0.5])
+
+
+WS = ctypes.c_void_p(0x400000)      # 256-byte aligned device workspace, never dereferenced
+
+
+def hst(L, q=A, k=A, v=A, o=A2, it=1, ot=0, b=1, H=2, N=256, dk=64, dv=64, chunk=64, g=None,
+        si=None, so=None, seg=128, ws=WS, wsb=None):
+    g = G(0.9, 0.5) if g is None else g
+    if wsb is None:
+        wsb = L.retention_chunkwise_host_workspace_bytes(it, ot, b, H, dk, dv, seg)
+    return L.retention_chunkwise_host(q, k, v, o, it, ot, b, H, N, dk, dv, chunk, g, si, so, seg,
+                                      ws, wsb, S, S, S)
+
+
+def test_chunkwise_host_workspace_size(L):
+    f = L.retention_chunkwise_host_workspace_bytes
+    # fp32 state 2*64*64*4 = 32 KB, then per buffer set q, k (bf16 2*128*64*2 = 32 KB each),
+    # v (32 KB) and o (fp32, 64 KB), two sets
+    assert f(1, 0, 1, 2, 64, 64, 128) == 32768 + 2 * (32768 * 3 + 65536)
+    assert f(1, 1, 1, 2, 64, 64, 128) == 32768 + 2 * (32768 * 4)
+    assert f(1, 0, 1, 3, 16, 16, 16) % 256 == 0                       # every part 256-aligned
+    assert f(7, 0, 1, 2, 64, 64, 128) == 0
+    assert f(1, 0, -1, 2, 64, 64, 128) == 0
+
+
+def test_chunkwise_host_rejections(L):
+    before = binding.kernel_launches()
+    assert hst(L, seg=96) == binding.RET_ERR_SHAPE                    # not a multiple of chunk
+    assert hst(L, seg=192) == binding.RET_ERR_SHAPE                   # does not divide N
+    assert hst(L, seg=0) == binding.RET_ERR_SHAPE
+    assert hst(L, wsb=1024) == binding.RET_ERR_SHAPE                  # workspace too small
+    assert hst(L, ws=ctypes.c_void_p(0x400010)) == binding.RET_ERR_ALIGN
+    assert hst(L, q=MIS) == binding.RET_ERR_ALIGN
+    assert hst(L, si=MIS) == binding.RET_ERR_ALIGN
+    assert hst(L, ws=NUL) == binding.RET_ERR_NULL
+    assert hst(L, o=NUL) == binding.RET_ERR_NULL
+    assert hst(L, it=4) == binding.RET_ERR_DTYPE
+    assert hst(L, dk=24) == binding.RET_ERR_UNSUPPORTED
+    assert hst(L, g=G(0.9, 1.2)) == binding.RET_ERR_UNSUPPORTED
+    assert hst(L, N=200) == binding.RET_ERR_SHAPE                     # N % chunk
+    assert hst(L, b=0, q=NUL, k=NUL, v=NUL, o=NUL) == binding.RET_OK
+    assert binding.kernel_launches() == before
