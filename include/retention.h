@@ -139,6 +139,25 @@ size_t retention_chunkwise_host_workspace_bytes(ret_dtype in_dtype, ret_dtype ou
                                                 int H, int dk, int dv, int seg_len);
 
 /*
+ * retention_chunkwise_host without a caller workspace: the carried state and the segment
+ * buffers live in a file-scope device array of retention_chunkwise_host_static_scratch_bytes()
+ * bytes, reserved on each device when the library's module loads there; its address is
+ * looked up once per device.  Arguments and behaviour otherwise as retention_chunkwise_host.
+ * A call whose workspace (retention_chunkwise_host_workspace_bytes) exceeds the scratch
+ * returns RET_ERR_SHAPE, like every other argument check, before any device access.  The
+ * scratch is shared by all calls on a device: they must not overlap in time (issue them
+ * on one stream, or synchronise between them).
+ */
+int retention_chunkwise_host_noalloc(const void* q, const void* k, const void* v, void* o,
+                                     ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                                     int dk, int dv, int chunk, const double* gamma,
+                                     const float* state_in, float* state_out, int seg_len,
+                                     void* stream, void* h2d_stream, void* d2h_stream);
+
+/* Bytes of the static scratch behind retention_chunkwise_host_noalloc.  Host-side. */
+size_t retention_chunkwise_host_static_scratch_bytes(void);
+
+/*
  * One decode step of the recurrent form, [RN2] "Retention" 2) eq.(6) and the
  * inference paragraph of "訓練/推理" (O(1) state per token):
  *   S <- gamma_h S + k^T v     (in place, fp32)

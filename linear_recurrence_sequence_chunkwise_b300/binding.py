@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
                                                    vp, vp, i, vp, ctypes.c_size_t, vp, vp, vp]
             L.retention_chunkwise_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
             L.retention_chunkwise_host_workspace_bytes.restype = ctypes.c_size_t
+            L.retention_chunkwise_host_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i,
+                                                           dp, vp, vp, i, vp, vp, vp]
+            L.retention_chunkwise_host_static_scratch_bytes.argtypes = []
+            L.retention_chunkwise_host_static_scratch_bytes.restype = ctypes.c_size_t
             L.retention_status_string.argtypes = [i]
             L.retention_status_string.restype = ctypes.c_char_p
             L.retention_check_device_error.argtypes = [vp]
@@ -79,7 +83,8 @@ def lib() -> ctypes.CDLL:
             L.retention_cuda_error_string.restype = ctypes.c_char_p
             for name in ("retention_parallel", "retention_chunkwise", "retention_recurrent_step",
                          "msr_epilogue", "retention_check_device_error",
-                         "retention_parallel_gated", "retention_chunkwise_host"):
+                         "retention_parallel_gated", "retention_chunkwise_host",
+                         "retention_chunkwise_host_noalloc"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -206,6 +211,33 @@ def retention_chunkwise_host(q, k, v, gamma, chunk: int, out, seg_len: int, stat
         ctypes.c_size_t(workspace.numel()), _stream(stream),
         ctypes.c_void_p(copy_streams[0].cuda_stream), ctypes.c_void_p(copy_streams[1].cuda_stream))
     _check("retention_chunkwise_host", rc)
+    return out
+
+
+def chunkwise_host_static_scratch_bytes() -> int:
+    return int(lib().retention_chunkwise_host_static_scratch_bytes())
+
+
+def retention_chunkwise_host_noalloc(q, k, v, gamma, chunk: int, out, seg_len: int,
+                                     state_in=None, state_out=None, stream=None,
+                                     copy_streams=None):
+    """retention_chunkwise_host on the library's static device scratch (no workspace);
+    calls on one device must not overlap in time."""
+    b, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if copy_streams is None:
+        if dev.index not in _copy_streams:
+            _copy_streams[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        copy_streams = _copy_streams[dev.index]
+    rc = lib().retention_chunkwise_host_noalloc(
+        _host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(out), _dtype_code(q.dtype),
+        _dtype_code(out.dtype), b, H, N, dk, dv, chunk, _gamma(gamma, H), _ptr(state_in),
+        _ptr(state_out), seg_len, _stream(stream), ctypes.c_void_p(copy_streams[0].cuda_stream),
+        ctypes.c_void_p(copy_streams[1].cuda_stream))
+    _check("retention_chunkwise_host_noalloc", rc)
     return out
 
 

@@ -9,6 +9,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -38,6 +40,63 @@ bool valid_dtype(int d) { return d == RET_F32 || d == RET_BF16; }
 
 int status_of(cudaError_t e) { return ret::record_cuda_status(e); }
 
+// Every argument check of retention_chunkwise_host (host-side, no GPU access).  Returns
+// RET_OK to proceed, kNoWork when b, H or N is zero, or the status to return.
+constexpr int kNoWork = -1;
+int check_args(const void* q, const void* k, const void* v, const void* o, int in_dtype,
+               int out_dtype, int b, int H, int N, int dk, int dv, int chunk, const double* gamma,
+               const float* state_in, const float* state_out, int seg_len, const void* workspace,
+               size_t workspace_bytes) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (dk <= 0 || dv <= 0 || dk % 16 || dv % 16 || dk > 256 || dv > 512) return RET_ERR_UNSUPPORTED;
+    if (chunk < 16 || chunk > 256 || chunk % 16 != 0 || N % chunk != 0) return RET_ERR_SHAPE;
+    if (seg_len <= 0 || seg_len % chunk != 0 || N % seg_len != 0) return RET_ERR_SHAPE;
+    if (H > ret::kMaxHeads) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || H == 0) return kNoWork;
+    if (!gamma) return RET_ERR_NULL;
+    for (int h = 0; h < H; ++h)
+        if (!(gamma[h] >= 0.0 && gamma[h] <= 1.0)) return RET_ERR_UNSUPPORTED;
+    if (N == 0) return kNoWork;
+    if (!q || !k || !v || !o || !workspace) return RET_ERR_NULL;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((mis & 15u) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return RET_ERR_ALIGN;
+    if ((state_in && (reinterpret_cast<uintptr_t>(state_in) & 15u)) ||
+        (state_out && (reinterpret_cast<uintptr_t>(state_out) & 15u)))
+        return RET_ERR_ALIGN;
+    if (workspace_bytes < layout(in_dtype, out_dtype, b, H, dk, dv, seg_len).total())
+        return RET_ERR_SHAPE;
+    return RET_OK;
+}
+
+// Scratch of the no-allocation entry point: a file-scope device array, reserved when the
+// library's module loads on a device, so calls need no workspace from the caller.
+constexpr size_t kStaticScratchBytes = size_t(48) << 20;
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_static_scratch on the current device, looked up once per device.
+cudaError_t static_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        e = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
+        if (e != cudaSuccess) {
+            addr[dev] = nullptr;
+            return e;
+        }
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -56,29 +115,15 @@ int retention_chunkwise_host(const void* q, const void* k, const void* v, void* 
                              float* state_out, int seg_len, void* workspace,
                              size_t workspace_bytes, void* stream, void* h2d_stream,
                              void* d2h_stream) {
-    // ---- every check before the first copy
-    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
-    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return RET_ERR_DTYPE;
-    if (dk <= 0 || dv <= 0 || dk % 16 || dv % 16 || dk > 256 || dv > 512) return RET_ERR_UNSUPPORTED;
-    if (chunk < 16 || chunk > 256 || chunk % 16 != 0 || N % chunk != 0) return RET_ERR_SHAPE;
-    if (seg_len <= 0 || seg_len % chunk != 0 || N % seg_len != 0) return RET_ERR_SHAPE;
-    if (H > ret::kMaxHeads) return RET_ERR_UNSUPPORTED;
-    if (b == 0 || H == 0) return RET_OK;
-    if (!gamma) return RET_ERR_NULL;
-    for (int h = 0; h < H; ++h)
-        if (!(gamma[h] >= 0.0 && gamma[h] <= 1.0)) return RET_ERR_UNSUPPORTED;
-    if (N == 0)   // no tokens: retention_chunkwise hands state_in to state_out
-        return retention_chunkwise(nullptr, nullptr, nullptr, nullptr, in_dtype, out_dtype, b, H,
-                                   0, dk, dv, chunk, gamma, state_in, state_out, stream);
-    if (!q || !k || !v || !o || !workspace) return RET_ERR_NULL;
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-    if ((mis & 15u) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return RET_ERR_ALIGN;
-    if ((state_in && (reinterpret_cast<uintptr_t>(state_in) & 15u)) ||
-        (state_out && (reinterpret_cast<uintptr_t>(state_out) & 15u)))
-        return RET_ERR_ALIGN;
+    const int rc = check_args(q, k, v, o, in_dtype, out_dtype, b, H, N, dk, dv, chunk, gamma,
+                              state_in, state_out, seg_len, workspace, workspace_bytes);
+    if (rc == kNoWork)   // zero sizes; with no tokens retention_chunkwise hands the state over
+        return (N == 0 && b > 0 && H > 0)
+                   ? retention_chunkwise(nullptr, nullptr, nullptr, nullptr, in_dtype, out_dtype, b,
+                                         H, 0, dk, dv, chunk, gamma, state_in, state_out, stream)
+                   : RET_OK;
+    if (rc != RET_OK) return rc;
     const Layout L = layout(in_dtype, out_dtype, b, H, dk, dv, seg_len);
-    if (workspace_bytes < L.total()) return RET_ERR_SHAPE;
 
     // ---- workspace: carried state, then two buffer sets (q, k, v, o) of one segment each
     uint8_t* base = static_cast<uint8_t*>(workspace);
@@ -167,6 +212,29 @@ int retention_chunkwise_host(const void* q, const void* k, const void* v, void* 
         e = cudaMemcpyAsync(state_out, st, (size_t)b * H * dk * dv * sizeof(float),
                             cudaMemcpyDeviceToDevice, cs);
     return finish(status_of(e));
+}
+
+size_t retention_chunkwise_host_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+int retention_chunkwise_host_noalloc(const void* q, const void* k, const void* v, void* o,
+                                     ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                                     int dk, int dv, int chunk, const double* gamma,
+                                     const float* state_in, float* state_out, int seg_len,
+                                     void* stream, void* h2d_stream, void* d2h_stream) {
+    // every check, the size of the static scratch included, before any device access (the
+    // placeholder stands for the scratch address, which is 256-byte aligned)
+    const int rc = check_args(q, k, v, o, in_dtype, out_dtype, b, H, N, dk, dv, chunk, gamma,
+                              state_in, state_out, seg_len, reinterpret_cast<const void*>(kAlign),
+                              kStaticScratchBytes);
+    if (rc != RET_OK && rc != kNoWork) return rc;
+    void* scratch = nullptr;
+    if (rc == RET_OK) {
+        const cudaError_t e = static_scratch(&scratch);
+        if (e != cudaSuccess) return status_of(e);
+    }
+    return retention_chunkwise_host(q, k, v, o, in_dtype, out_dtype, b, H, N, dk, dv, chunk, gamma,
+                                    state_in, state_out, seg_len, scratch, kStaticScratchBytes,
+                                    stream, h2d_stream, d2h_stream);
 }
 
 }  // extern "C"

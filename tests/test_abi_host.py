@@ -35,7 +35,9 @@ def test_exports_every_declared_function(L):
                           "retention_check_device_error", "retention_kernel_launches",
                           "retention_last_kernel", "retention_last_cuda_error",
                           "retention_cuda_error_string", "retention_parallel_gated",
-                          "retention_chunkwise_host", "retention_chunkwise_host_workspace_bytes"}
+                          "retention_chunkwise_host", "retention_chunkwise_host_workspace_bytes",
+                          "retention_chunkwise_host_noalloc",
+                          "retention_chunkwise_host_static_scratch_bytes"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
