@@ -95,6 +95,12 @@ __device__ __forceinline__ void fail(volatile int* abort_flag) {
     atomicOr(&g_err_parallel, 1u);
 }
 
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
@@ -509,9 +515,11 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                             const int ch_ = head * dv + col + 32 * hf + jj;
                             if (ea.weight) yn *= ea.weight[ch_];
                             if (ea.bias) yn += ea.bias[ch_];
-                            // swish with the hardware exp2/reciprocal paths (a few ulp, far
-                            // inside the bf16-input tolerance); g -> -inf gives g * 0 = -0
-                            o[jj] = __fdividef(gv[jj], 1.0f + __expf(-gv[jj])) * yn;
+                            // swish(g) = g sigmoid(g) = h (1 + tanh(h)), h = g / 2, with the
+                            // hardware tanh (one special-function op; relative error near
+                            // 2^-11, far inside the bf16-input tolerance)
+                            const float hg = 0.5f * gv[jj];
+                            o[jj] = fmaf(hg, tanh_approx(hg), hg) * yn;
                         }
                     }
                     if (OUT_BF16) {
