@@ -112,8 +112,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int NH, int NV, bool OUT_BF16, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
-                   const __grid_constant__ CUtensorMap mg, int N, int H, int dk, int dv, int bH,
+                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg, int N, int H, int dk, int dv, int bH,
                    int nvb, unsigned flags, const ParConsts pc, const EpiArgs ea) {
     constexpr int W = 128 * NV;
     constexpr int kEpiChunks = W / 128;                   // 64-column chunks per group
@@ -570,8 +569,8 @@ parallel_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 namespace {
 
 using ParKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                           const CUtensorMap, const CUtensorMap, int, int, int, int, int, int,
-                           unsigned, const ParConsts, const EpiArgs);
+                           const CUtensorMap, int, int, int, int, int, int, unsigned,
+                           const ParConsts, const EpiArgs);
 
 template <int EPI>
 ParKernel pick(int nh, int nv, int out_bf16) {
@@ -606,18 +605,15 @@ cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, 
     }
     const long long bH = (long long)b * H;
     if (bH >= (1LL << 31) || N >= (1 << 30)) return cudaErrorNotSupported;
-    CUtensorMap mq, mk, mv, mo, mg;
+    CUtensorMap mq, mk, mv, mg;
     if (!make_map_bf16_3d(&mq, q, bH, N, dk, 128) || !make_map_bf16_3d(&mk, k, bH, N, dk, 128) ||
         !make_map_bf16_3d(&mv, v, bH, N, dv, 128))
         return cudaErrorInvalidValue;
-    // outputs (and the gate) move through 128-byte-wide boxes of 128 rows
+    // the gate moves through 128-byte-wide boxes of 128 rows (unused without the epilogue)
     if (epi == 0) {
-        if (!make_map_3d_128b(&mo, o, out_bf16 != 0, bH, N, dv, 128)) return cudaErrorInvalidValue;
-        mg = mo;
-    } else {
-        if (!make_map_3d_128b(&mo, o, out_bf16 != 0, b, N, (uint64_t)H * dv, 128) ||
-            !make_map_3d_128b(&mg, ea.g, epi == 2, b, N, (uint64_t)H * dv, 128))
-            return cudaErrorInvalidValue;
+        mg = mq;
+    } else if (!make_map_3d_128b(&mg, ea.g, epi == 2, b, N, (uint64_t)H * dv, 128)) {
+        return cudaErrorInvalidValue;
     }
     const long long grid = (long long)((N + 127) / 128) * bH * nvb;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -641,7 +637,7 @@ cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mg, N, H, dk, dv, (int)bH, nvb, flags, pc, ea);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mg, N, H, dk, dv, (int)bH, nvb, flags, pc, ea);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(epi == 0 ? RET_KERNEL_PARALLEL_TC : RET_KERNEL_PARALLEL_GATED_TC);
     return e;

@@ -58,8 +58,8 @@ inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t planes
 }
 
 // Map over a bf16 or fp32 tensor [planes][rows][cols] whose boxes are 128 bytes wide
-// (64 bf16 or 32 fp32 columns) by box_rows rows, 128-byte swizzle; used for staged
-// epilogue loads and stores.
+// (64 bf16 or 32 fp32 columns) by box_rows rows, 128-byte swizzle; used for the gate
+// tiles of the fused epilogue.
 inline bool make_map_3d_128b(CUtensorMap* map, const void* base, bool bf16, uint64_t planes,
                              uint64_t rows, uint64_t cols, uint32_t box_rows) {
     auto fn = encode_fn();
