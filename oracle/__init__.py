@@ -82,8 +82,10 @@ class Oracle:
         lib.oracle_chunkwise.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P]
         lib.oracle_brute.argtypes = [P, P, P, P, I, I, I, I, I, P]
         lib.oracle_msr_epilogue.argtypes = [P, P, P, I, I, I, I, ctypes.c_double, P, P]
+        lib.oracle_chunkwise_backward.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, P]
         for f in ("oracle_parallel", "oracle_recurrent", "oracle_recurrent_step",
-                  "oracle_chunkwise", "oracle_brute", "oracle_msr_epilogue"):
+                  "oracle_chunkwise", "oracle_brute", "oracle_msr_epilogue",
+                  "oracle_chunkwise_backward"):
             getattr(lib, f).restype = ctypes.c_int
         self.lib = lib
 
@@ -142,6 +144,20 @@ class Oracle:
                "brute")
         return o
 
+    def chunkwise_backward(self, q, k, v, dout, gamma, state_in=None, dstate_out=None):
+        """Gradient of L = sum(dout * o) + <dstate_out, final state> for the chunkwise
+        form (any chunk length gives the same function).  Returns (dq, dk, dv, dstate_in)."""
+        q, k, v, do, g = _f64(q), _f64(k), _f64(v), _f64(dout), _f64(gamma)
+        b, H, N, dk = q.shape
+        dv = v.shape[-1]
+        si, ds = _f64(state_in), _f64(dstate_out)
+        gq, gk, gv = np.zeros((b, H, N, dk)), np.zeros((b, H, N, dk)), np.zeros((b, H, N, dv))
+        gs = np.zeros((b, H, dk, dv))
+        _check(self.lib.oracle_chunkwise_backward(_p(q), _p(k), _p(v), _p(do), _p(si), _p(ds),
+                                                  _p(gq), _p(gk), _p(gv), _p(gs), b, H, N, dk,
+                                                  dv, _p(g)), "chunkwise_backward")
+        return gq, gk, gv, gs
+
     def msr_epilogue(self, y, g, eps: float, weight=None, bias=None) -> np.ndarray:
         """GroupNorm per (token, head) then swish(G) gate; y:[b,H,N,dv] g:[b,N,H*dv]."""
         y, g = _f64(y), _f64(g)
@@ -183,6 +199,10 @@ def brute(*a, **kw):
 
 def msr_epilogue(*a, **kw):
     return default().msr_epilogue(*a, **kw)
+
+
+def chunkwise_backward(*a, **kw):
+    return default().chunkwise_backward(*a, **kw)
 
 
 def map_units(fn, units, threads: int | None = None):

@@ -306,3 +306,95 @@ int oracle_msr_epilogue(const double* y, const double* g, double* out, int b, in
             }
     return 0;
 }
+
+/*
+ * Gradient of the chunkwise form.  [RN2] "訓練/推理" says training runs the
+ * parallel and chunkwise forms; the pages print no backward pass, so this is the
+ * exact derivative of what eq.(7) computes.  For every chunk length eq.(7) gives,
+ * per (batch, head), with S0 the incoming state (zero when state_in is NULL):
+ *   o_n     = gamma^(n+1) q_n S0 + sum_{m<=n} gamma^(n-m) (q_n . k_m) v_m
+ *   S_final = gamma^N S0 + sum_m gamma^(N-1-m) k_m^T v_m
+ * and the scalar  L = sum_n dout_n . o_n + <dstate_out, S_final>  (dstate_out NULL
+ * means zero).  Its partial derivatives, written out entry by entry:
+ *   dq_n[a] = sum_{m<=n} gamma^(n-m) (dout_n . v_m) k_m[a]
+ *             + gamma^(n+1) sum_c dout_n[c] S0[a][c]
+ *   dk_m[a] = sum_{n>=m} gamma^(n-m) (dout_n . v_m) q_n[a]
+ *             + gamma^(N-1-m) sum_c dstate_out[a][c] v_m[c]
+ *   dv_m[c] = sum_{n>=m} gamma^(n-m) (q_n . k_m) dout_n[c]
+ *             + gamma^(N-1-m) sum_a k_m[a] dstate_out[a][c]
+ *   dS0[a][c] = sum_n gamma^(n+1) q_n[a] dout_n[c] + gamma^N dstate_out[a][c]
+ * Layouts as above; dout like o, dq/dk like q, dv like v, dstate_in and
+ * dstate_out like state.  dstate_in may be NULL (not computed).
+ */
+int oracle_chunkwise_backward(const double* q, const double* k, const double* v,
+                              const double* dout, const double* state_in,
+                              const double* dstate_out, double* dq, double* dk, double* dv,
+                              double* dstate_in, int b, int H, int N, int dk_, int dv_,
+                              const double* gamma) {
+    if (b < 0 || H < 0 || N < 0 || dk_ <= 0 || dv_ <= 0) return -1;
+    size_t SS = (size_t)dk_ * dv_;
+    for (int bi = 0; bi < b; ++bi)
+        for (int h = 0; h < H; ++h) {
+            size_t u = (size_t)bi * H + h;
+            const double* Q = q + u * (size_t)N * dk_;
+            const double* K = k + u * (size_t)N * dk_;
+            const double* V = v + u * (size_t)N * dv_;
+            const double* DO = dout + u * (size_t)N * dv_;
+            const double* S0 = state_in ? state_in + u * SS : NULL;
+            const double* DS = dstate_out ? dstate_out + u * SS : NULL;
+            double g = gamma[h];
+            for (int n = 0; n < N; ++n) {
+                const double* don = DO + (size_t)n * dv_;
+                double* dqn = dq + (u * N + n) * dk_;
+                for (int a = 0; a < dk_; ++a) dqn[a] = 0.0;
+                for (int m = 0; m <= n; ++m) {
+                    double w = gpow(g, n - m) * dot(don, V + (size_t)m * dv_, dv_);
+                    const double* km = K + (size_t)m * dk_;
+                    for (int a = 0; a < dk_; ++a) dqn[a] += w * km[a];
+                }
+                if (S0) {
+                    double f = gpow(g, n + 1);
+                    for (int a = 0; a < dk_; ++a)
+                        dqn[a] += f * dot(don, S0 + (size_t)a * dv_, dv_);
+                }
+            }
+            for (int m = 0; m < N; ++m) {
+                const double* km = K + (size_t)m * dk_;
+                const double* vm = V + (size_t)m * dv_;
+                double* dkm = dk + (u * N + m) * dk_;
+                double* dvm = dv + (u * N + m) * dv_;
+                for (int a = 0; a < dk_; ++a) dkm[a] = 0.0;
+                for (int c = 0; c < dv_; ++c) dvm[c] = 0.0;
+                for (int n = m; n < N; ++n) {
+                    double gd = gpow(g, n - m);
+                    const double* qn = Q + (size_t)n * dk_;
+                    const double* don = DO + (size_t)n * dv_;
+                    double wk = gd * dot(don, vm, dv_);
+                    double wv = gd * dot(qn, km, dk_);
+                    for (int a = 0; a < dk_; ++a) dkm[a] += wk * qn[a];
+                    for (int c = 0; c < dv_; ++c) dvm[c] += wv * don[c];
+                }
+                if (DS) {
+                    double f = gpow(g, N - 1 - m);
+                    for (int a = 0; a < dk_; ++a)
+                        dkm[a] += f * dot(DS + (size_t)a * dv_, vm, dv_);
+                    for (int c = 0; c < dv_; ++c) {
+                        double s = 0.0;
+                        for (int a = 0; a < dk_; ++a) s += km[a] * DS[(size_t)a * dv_ + c];
+                        dvm[c] += f * s;
+                    }
+                }
+            }
+            if (dstate_in) {
+                double* D0 = dstate_in + u * SS;
+                for (int a = 0; a < dk_; ++a)
+                    for (int c = 0; c < dv_; ++c) {
+                        double s = DS ? gpow(g, N) * DS[(size_t)a * dv_ + c] : 0.0;
+                        for (int n = 0; n < N; ++n)
+                            s += gpow(g, n + 1) * Q[(size_t)n * dk_ + a] * DO[(size_t)n * dv_ + c];
+                        D0[(size_t)a * dv_ + c] = s;
+                    }
+            }
+        }
+    return 0;
+}
