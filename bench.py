@@ -364,6 +364,41 @@ def bench_parallel(args, dist, rb, pk):
                          "algorithmic_flops_per_launch": flops}}
 
 
+# fp32 FMA lanes: 148 SMs x 128 lanes, 2 flop per FMA, at the maximum SM clock
+FP32_LANES = 148 * 128
+
+
+def bench_backward(args, dist, rb, pk):
+    w = inputs.BACKWARD
+    q, k, v = inputs.qkv(w, "cuda")
+    do = inputs.dout(w, "cuda")
+    grads = tuple(torch.empty(w.b, w.H, w.N, d, dtype=torch.float32, device="cuda")
+                  for d in (w.dk, w.dk, w.dv))
+
+    def step():
+        # one kernel: dq (forward scan), dk and dv (reverse scans) side by side
+        rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk, grads=grads)
+
+    steps = max(3, args.steps // 10)
+    ms, _ = timed(step, steps, 3, dist)
+    rb.check_device_error()
+    ms_step = ms / steps
+    value, _ = aggregate(dist, ms, w.b * w.N * steps)
+    flops = inputs.algorithmic_flops("backward", w)
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    peak = 2.0 * FP32_LANES * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    del q, k, v, do, grads
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: gradient of chunkwise retention b{w.b} H{w.H} N{w.N} "
+                        f"dk{w.dk} dv{w.dv} chunk {w.chunk}, bf16 q/k/v/dout N(0,1)/16, fp32 "
+                        "dq/dk/dv (retention_chunkwise_backward, CUDA-core kernel)",
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "peak_basis": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x max SM clock"}}
+
+
 def cpu_baseline_leg():
     w = inputs.CHUNKWISE_LONG
     threads = max(1, min(os.cpu_count() or 1, w.H))
@@ -382,6 +417,7 @@ def run_ours(args, dist: Dist):
     if not args.only_headline:
         extra["decode"] = bench_decode(args, dist, rb, pk)
         extra["parallel"] = bench_parallel(args, dist, rb, pk)
+        extra["backward"] = bench_backward(args, dist, rb, pk)
     cpu = cpu_baseline_leg() if (dist.rank == 0 and dist.world == 1 and not args.no_cpu) else None
     if dist.rank != 0:
         return 0
@@ -405,6 +441,7 @@ PROFILE_CASES = {
     "chunkwise": "chunkwise_long at N=8192: b1 H16 dk256 dv512 chunk 256, bf16 in, fp32 out",
     "decode": "decode at b32: H16 dk256 dv512, fp32 state (268 MB), bf16 q/k/v, fp32 out",
     "parallel": "parallel_norm (b8 H8 N2048 dk256 dv512, all normalisations) + epilogue",
+    "backward": "backward (b4 H16 N2048 dk256 dv512 chunk 64), bf16 in, fp32 gradients (1.1 GB)",
 }
 
 
@@ -425,6 +462,14 @@ def run_profile(case: str) -> int:
                       for i, d in enumerate((w.dk, w.dk, w.dv)))
         o = torch.empty(32, w.H, w.dv, dtype=torch.float32, device="cuda")
         calls = [lambda: rb.retention_recurrent_step(qs, ks, vs, state, w.gamma, out=o)]
+    elif case == "backward":
+        w = inputs.BACKWARD
+        q, k, v = inputs.qkv(w, "cuda")
+        do = inputs.dout(w, "cuda")
+        grads = tuple(torch.empty(w.b, w.H, w.N, d, dtype=torch.float32, device="cuda")
+                      for d in (w.dk, w.dk, w.dv))
+        calls = [lambda: rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk,
+                                                         grads=grads)]
     else:
         w = inputs.PARALLEL_NORM
         q, k, v = inputs.qkv(w, "cuda")

@@ -98,6 +98,33 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
                         const float* state_in, float* state_out, void* stream);
 
 /*
+ * Gradient of retention_chunkwise.  [RN2] "訓練/推理" trains with the parallel and
+ * chunkwise forms; the pages print no backward pass, so this is the exact derivative
+ * of eq.(7) ([RN2] "Retention" 3)), which is the same function for every chunk length.
+ * With S0 = state_in (NULL means zero) and the scalar
+ *   L = sum_n dout_n . o_n + <dstate_out, S_final>      (dstate_out NULL means zero)
+ * the call writes
+ *   grad_q[n] = sum_{m<=n} gamma^(n-m) (dout_n . v_m) k_m + gamma^(n+1) dout_n S0^T
+ *   grad_k[m] = sum_{n>=m} gamma^(n-m) (dout_n . v_m) q_n + gamma^(N-1-m) v_m dstate_out^T
+ *   grad_v[m] = sum_{n>=m} gamma^(n-m) (q_n . k_m) dout_n + gamma^(N-1-m) k_m dstate_out
+ *   dstate_in = sum_n gamma^(n+1) q_n^T dout_n + gamma^N dstate_out   (if not NULL)
+ * computed chunk by chunk: grad_q by the forward scan of eq.(7) with (q, k, v) replaced
+ * by (dout, v, k); grad_k and grad_v by the same scan run from the last chunk to the
+ * first with the carried gradient of the state.  One CUDA-core kernel launch.
+ * q, k: [b][H][N][dk], v, dout: [b][H][N][dv], all in in_dtype; grad_q, grad_k:
+ * [b][H][N][dk] and grad_v: [b][H][N][dv] in out_dtype (written; must not overlap the
+ * inputs); state_in, dstate_out, dstate_in: [b][H][dk][dv] fp32, nullable
+ * (dstate_in must not overlap the others).  All DEVICE pointers.  Shapes and
+ * errors as in retention_chunkwise; N = 0 writes dstate_in = dstate_out (or zero).
+ */
+int retention_chunkwise_backward(const void* q, const void* k, const void* v,
+                                 const void* dout, void* grad_q, void* grad_k, void* grad_v,
+                                 ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                                 int dk, int dv, int chunk, const double* gamma,
+                                 const float* state_in, const float* dstate_out,
+                                 float* dstate_in, void* stream);
+
+/*
  * retention_chunkwise over HOST-resident inputs and outputs.  The sequence passes
  * through the device in segments of seg_len tokens (a multiple of chunk dividing N);
  * eq.(7) carries the state across any split at a chunk boundary ([RN2] "Retention" 3)),
@@ -241,7 +268,8 @@ enum {
     RET_KERNEL_CHUNKWISE_TC = 5,    /* chunkwise form, tcgen05 tensor-core kernel     */
     RET_KERNEL_PARALLEL_TC = 6,     /* parallel form, tcgen05 tensor-core kernel      */
     RET_KERNEL_PARALLEL_GATED_TC = 7, /* parallel form + gated GroupNorm, tensor cores */
-    RET_KERNEL_CHUNKWISE_TC_PAIR = 8  /* chunkwise form, tensor cores on pairs of SMs */
+    RET_KERNEL_CHUNKWISE_TC_PAIR = 8, /* chunkwise form, tensor cores on pairs of SMs */
+    RET_KERNEL_CHUNKWISE_BACKWARD_SIMT = 9 /* chunkwise gradient, CUDA-core fp32 FMA    */
 };
 
 /*

@@ -24,7 +24,8 @@ RET_F32, RET_BF16 = 0, 1
 NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
-                5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair"}
+                5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair",
+                9: "chunkwise_backward_simt"}
 
 _lib = None
 _lock = threading.Lock()
@@ -58,6 +59,8 @@ def lib() -> ctypes.CDLL:
             dp = ctypes.POINTER(ctypes.c_double)
             L.retention_parallel.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, dp, u, vp]
             L.retention_chunkwise.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp, vp, vp, vp]
+            L.retention_chunkwise_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                                       i, i, i, dp, vp, vp, vp, vp]
             L.retention_recurrent_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, dp, vp]
             L.msr_epilogue.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, vp]
             L.retention_parallel_gated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp,
@@ -168,6 +171,35 @@ def retention_chunkwise(q, k, v, gamma, chunk: int, state_in=None, state_out=Non
                                    _stream(stream))
     _check("retention_chunkwise", rc)
     return out
+
+
+def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None,
+                                 dstate_out=None, dstate_in=None, grads=None,
+                                 out_dtype=torch.float32, stream=None):
+    """Gradient of retention_chunkwise for L = sum(dout * o) + <dstate_out, final state>.
+
+    Returns (grad_q, grad_k, grad_v, dstate_in); dstate_in is None unless a tensor is
+    passed (fp32 [b,H,dk,dv]).  grads: optional preallocated (grad_q, grad_k, grad_v)."""
+    b, H, N, dk = q.shape
+    dv = v.shape[-1]
+    if k.dtype != q.dtype or v.dtype != q.dtype or dout.dtype != q.dtype:
+        raise TypeError("q, k, v and dout must share one dtype")
+    for s in (state_in, dstate_out, dstate_in):
+        if s is not None and s.dtype != torch.float32:
+            raise TypeError("states are fp32")
+    if grads is None:
+        grads = (torch.empty((b, H, N, dk), dtype=out_dtype, device=q.device),
+                 torch.empty((b, H, N, dk), dtype=out_dtype, device=q.device),
+                 torch.empty((b, H, N, dv), dtype=out_dtype, device=q.device))
+    gq, gk, gv = grads
+    if gk.dtype != gq.dtype or gv.dtype != gq.dtype:
+        raise TypeError("the three gradients must share one dtype")
+    rc = lib().retention_chunkwise_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(gq), _ptr(gk), _ptr(gv),
+        _dtype_code(q.dtype), _dtype_code(gq.dtype), b, H, N, dk, dv, chunk, _gamma(gamma, H),
+        _ptr(state_in), _ptr(dstate_out), _ptr(dstate_in), _stream(stream))
+    _check("retention_chunkwise_backward", rc)
+    return gq, gk, gv, dstate_in
 
 
 _copy_streams = {}

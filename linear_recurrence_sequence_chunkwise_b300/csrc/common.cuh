@@ -81,6 +81,12 @@ cudaError_t launch_chunkwise_simt(const void* q, const void* k, const void* v, v
                                   int in_bf16, int out_bf16, int b, int H, int N, int dk,
                                   int dv, int chunk, const HeadConsts& hc,
                                   const float* state_in, float* state_out, cudaStream_t s);
+cudaError_t launch_chunkwise_backward_simt(const void* q, const void* k, const void* v,
+                                           const void* dout, void* dq, void* dk, void* dv,
+                                           int in_bf16, int out_bf16, int b, int H, int N,
+                                           int dkk, int dvv, int chunk, const HeadConsts& hc,
+                                           const float* state_in, const float* dstate_out,
+                                           float* dstate_in, cudaStream_t s);
 // Tensor-core paths: return cudaErrorNotSupported when the shape is outside
 // what the kernel handles, so the caller can pick the CUDA-core kernel.
 cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, void* o,

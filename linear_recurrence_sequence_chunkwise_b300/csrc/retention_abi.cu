@@ -172,6 +172,46 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
                                                   dk, dv, chunk, hc, state_in, state_out, s));
 }
 
+int retention_chunkwise_backward(const void* q, const void* k, const void* v,
+                                 const void* dout, void* grad_q, void* grad_k, void* grad_v,
+                                 ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                                 int dk, int dv, int chunk, const double* gamma,
+                                 const float* state_in, const float* dstate_out,
+                                 float* dstate_in, void* stream) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (!dims_ok(dk, dv)) return RET_ERR_UNSUPPORTED;
+    if (chunk < 16 || chunk > 256 || chunk % 16 != 0) return RET_ERR_SHAPE;
+    if (N % chunk != 0) return RET_ERR_SHAPE;
+    if (b == 0 || H == 0) return RET_OK;
+    if (!gamma) return RET_ERR_NULL;
+    if ((state_in && !aligned16(state_in)) || (dstate_out && !aligned16(dstate_out)) ||
+        (dstate_in && !aligned16(dstate_in)))
+        return RET_ERR_ALIGN;
+    HeadConsts hc;
+    int rc = head_consts(gamma, H, chunk, &hc);
+    if (rc != RET_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        // No tokens: L = <dstate_out, S0>, so the incoming state's gradient is dstate_out.
+        if (!dstate_in) return RET_OK;
+        size_t bytes = (size_t)b * H * dk * dv * sizeof(float);
+        if (dstate_out) {
+            if (dstate_out == dstate_in) return RET_OK;
+            return cuda_status(cudaMemcpyAsync(dstate_in, dstate_out, bytes,
+                                               cudaMemcpyDeviceToDevice, s));
+        }
+        return cuda_status(cudaMemsetAsync(dstate_in, 0, bytes, s));
+    }
+    if (!q || !k || !v || !dout || !grad_q || !grad_k || !grad_v) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) ||
+        !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v))
+        return RET_ERR_ALIGN;
+    return cuda_status(ret::launch_chunkwise_backward_simt(
+        q, k, v, dout, grad_q, grad_k, grad_v, in_dtype == RET_BF16, out_dtype == RET_BF16, b,
+        H, N, dk, dv, chunk, hc, state_in, dstate_out, dstate_in, s));
+}
+
 int retention_recurrent_step(const void* q, const void* k, const void* v, float* state, void* o,
                              ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int dk,
                              int dv, const double* gamma, void* stream) {

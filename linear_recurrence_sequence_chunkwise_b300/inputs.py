@@ -14,6 +14,7 @@ synthetic):
   sweep           b4  H16 dk256 dv512 N in {2048,8192,16384} x chunk in {64,128,256}
   decode          b128 H16 dk256 dv512, state N(0, sigma=0.1), 512 steps of
                   bf16 q,k,v ~ N(0,1)/sqrt(dk)
+  backward        b4  H16 dk256 dv512 N2048   chunk 64   bf16 q,k,v,dout N(0,1)/sqrt(dk)
 Decay schedule: gamma_h = 1 - 2^(-5-h) (one fixed decay per head, as the
 multi-scale retention section prescribes; the schedule itself is a choice).
 """
@@ -67,7 +68,10 @@ SWEEP = [Workload(f"sweep_N{N}_B{B}", 4, 16, N, 256, 512, "bf16", 1.0 / 16.0, ch
 DECODE = Workload("decode", 128, 16, 1, 256, 512, "bf16", 1.0 / 16.0, steps=512,
                   state_std=0.1, seed=5000)
 
-WORKLOADS = {w.name: w for w in [TINY, PARALLEL_NORM, CHUNKWISE_LONG, DECODE] + SWEEP}
+# gradient of the chunkwise form at the first training-sweep shape; dout ~ N(0,1)/sqrt(dk)
+BACKWARD = Workload("backward", 4, 16, 2048, 256, 512, "bf16", 1.0 / 16.0, chunk=64, seed=6000)
+
+WORKLOADS = {w.name: w for w in [TINY, PARALLEL_NORM, CHUNKWISE_LONG, DECODE, BACKWARD] + SWEEP}
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -108,6 +112,12 @@ def qkv(w: Workload, device="cpu", N: int | None = None, seed_offset: int = 0):
     return q, k, v
 
 
+def dout(w: Workload, device="cpu", N: int | None = None) -> torch.Tensor:
+    """Upstream gradient of the output, [b,H,N,dv] in the storage dtype."""
+    N = w.N if N is None else N
+    return randn((w.b, w.H, N, w.dv), w.seed + 7, w.scale, w.dtype, device)
+
+
 def gate(w: Workload, device="cpu", N: int | None = None) -> torch.Tensor:
     """The swish gate input G = X W_G, token-major [b, N, H*dv], bf16 N(0,1)."""
     N = w.N if N is None else N
@@ -144,6 +154,10 @@ def algorithmic_flops(kind: str, w: Workload, N: int | None = None) -> float:
     chunkwise: per token per head, intra-chunk causal part (dk+dv)(B+1) plus the
                cross-chunk read and the state update, 2*dk*dv each.
     decode:    per (b,h) per step: state update 2*dk*dv, read-out 2*dk*dv.
+    backward:  per token per head, three causal intra-chunk parts (dq, dk, dv)
+               3 (dk+dv)(B+1), three cross-chunk reads 6*dk*dv and two carried
+               states (the forward one for dq, the gradient one shared by dk and dv)
+               4*dk*dv.
     """
     N = w.N if N is None else N
     if kind == "parallel":
@@ -153,6 +167,9 @@ def algorithmic_flops(kind: str, w: Workload, N: int | None = None) -> float:
         return float(w.b * w.H) * N * per_tok
     if kind == "decode":
         return float(w.b * w.H) * 4.0 * w.dk * w.dv
+    if kind == "backward":
+        per_tok = 3 * (w.dk + w.dv) * (w.chunk + 1) + 10 * w.dk * w.dv
+        return float(w.b * w.H) * N * per_tok
     raise ValueError(kind)
 
 

@@ -37,7 +37,8 @@ def test_exports_every_declared_function(L):
                           "retention_cuda_error_string", "retention_parallel_gated",
                           "retention_chunkwise_host", "retention_chunkwise_host_workspace_bytes",
                           "retention_chunkwise_host_noalloc",
-                          "retention_chunkwise_host_static_scratch_bytes"}
+                          "retention_chunkwise_host_static_scratch_bytes",
+                          "retention_chunkwise_backward"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
@@ -126,6 +127,37 @@ def test_chunkwise_rejections(L):
     assert chk(L, si=MIS) == binding.RET_ERR_ALIGN
     assert chk(L, so=MIS) == binding.RET_ERR_ALIGN
     assert chk(L, g=G(0.9, 1.01)) == binding.RET_ERR_UNSUPPORTED
+
+
+def bwd(L, q=A, k=A, v=A, do=A, gq=A2, gk=A2, gv=A2, it=1, ot=0, b=1, H=2, N=64, dk=64, dv=64,
+        chunk=16, g=None, si=None, ds=None, di=None):
+    g = G(0.9, 0.5) if g is None else g
+    return L.retention_chunkwise_backward(q, k, v, do, gq, gk, gv, it, ot, b, H, N, dk, dv, chunk,
+                                          g, si, ds, di, S)
+
+
+def test_chunkwise_backward_rejections(L):
+    before = binding.kernel_launches()
+    assert bwd(L, b=-1) == binding.RET_ERR_SHAPE
+    assert bwd(L, chunk=8) == binding.RET_ERR_SHAPE
+    assert bwd(L, N=100) == binding.RET_ERR_SHAPE
+    assert bwd(L, it=2) == binding.RET_ERR_DTYPE
+    assert bwd(L, ot=7) == binding.RET_ERR_DTYPE
+    assert bwd(L, dk=24) == binding.RET_ERR_UNSUPPORTED
+    assert bwd(L, dv=528) == binding.RET_ERR_UNSUPPORTED
+    assert bwd(L, do=NUL) == binding.RET_ERR_NULL
+    assert bwd(L, gv=NUL) == binding.RET_ERR_NULL
+    assert bwd(L, g=ctypes.POINTER(ctypes.c_double)()) == binding.RET_ERR_NULL
+    assert bwd(L, gk=MIS) == binding.RET_ERR_ALIGN
+    assert bwd(L, do=MIS) == binding.RET_ERR_ALIGN
+    assert bwd(L, di=MIS) == binding.RET_ERR_ALIGN
+    assert bwd(L, ds=MIS) == binding.RET_ERR_ALIGN
+    assert bwd(L, g=G(0.9, 1.5)) == binding.RET_ERR_UNSUPPORTED
+    assert bwd(L, H=129, g=G(*([0.5] * 129))) == binding.RET_ERR_UNSUPPORTED
+    # empty inputs: nothing to compute (no dstate_in requested)
+    assert bwd(L, b=0, q=NUL, k=NUL, v=NUL, do=NUL, gq=NUL, gk=NUL, gv=NUL) == binding.RET_OK
+    assert bwd(L, N=0, q=NUL, k=NUL, v=NUL, do=NUL, gq=NUL, gk=NUL, gv=NUL) == binding.RET_OK
+    assert binding.kernel_launches() == before
 
 
 def test_recurrent_step_rejections(L):
