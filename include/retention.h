@@ -110,7 +110,9 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
  *   dstate_in = sum_n gamma^(n+1) q_n^T dout_n + gamma^N dstate_out   (if not NULL)
  * computed chunk by chunk: grad_q by the forward scan of eq.(7) with (q, k, v) replaced
  * by (dout, v, k); grad_k and grad_v by the same scan run from the last chunk to the
- * first with the carried gradient of the state.  One CUDA-core kernel launch.
+ * first with the carried gradient of the state.  One CUDA-core kernel launch.  chunk is
+ * validated as in retention_chunkwise; since the result does not depend on it, the
+ * kernel scans in chunks of 64 tokens whenever N is a multiple of 64.
  * q, k: [b][H][N][dk], v, dout: [b][H][N][dv], all in in_dtype; grad_q, grad_k:
  * [b][H][N][dk] and grad_v: [b][H][N][dv] in out_dtype (written; must not overlap the
  * inputs); state_in, dstate_out, dstate_in: [b][H][dk][dv] fp32, nullable

@@ -188,8 +188,11 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
     if ((state_in && !aligned16(state_in)) || (dstate_out && !aligned16(dstate_out)) ||
         (dstate_in && !aligned16(dstate_in)))
         return RET_ERR_ALIGN;
+    // The gradient is the same function for every chunk length: scan in chunks of 64
+    // (the register-blocked kernel) whenever N allows it.
+    const int kchunk = (N % 64 == 0) ? 64 : chunk;
     HeadConsts hc;
-    int rc = head_consts(gamma, H, chunk, &hc);
+    int rc = head_consts(gamma, H, kchunk, &hc);
     if (rc != RET_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (N == 0) {
@@ -209,7 +212,7 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
         return RET_ERR_ALIGN;
     return cuda_status(ret::launch_chunkwise_backward_simt(
         q, k, v, dout, grad_q, grad_k, grad_v, in_dtype == RET_BF16, out_dtype == RET_BF16, b,
-        H, N, dk, dv, chunk, hc, state_in, dstate_out, dstate_in, s));
+        H, N, dk, dv, kchunk, hc, state_in, dstate_out, dstate_in, s));
 }
 
 int retention_recurrent_step(const void* q, const void* k, const void* v, float* state, void* o,

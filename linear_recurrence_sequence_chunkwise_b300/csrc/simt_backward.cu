@@ -189,6 +189,239 @@ chunkwise_backward_simt_kernel(const ScanArgs args, int H, int N, int B, const H
     }
 }
 
+// ---------------------------------------------------------------------------
+// Register-blocked variant for N a multiple of 64.  The gradient is the same
+// function for every chunk length, so this kernel scans in chunks of BT = 64 tokens
+// whatever chunk the caller validated.  Per chunk and 64-column slice the work is
+// four small products, each thread owning a 4x4 micro-tile (rows 4ty.., columns
+// 4tx..) and every operand staged k-major in shared memory so that one 16-byte
+// load feeds four FMAs:
+//   S  = X Y^T                       64 x 64, over dx in slabs of KS
+//   O  = X St                        64 x 64, same slabs (state as it entered the chunk)
+//   O  = cf (.) O + (S (.) decay) Z  decay and causal side applied in registers
+//   St = gamma^BT St + Y^T (w (.) Z) 64-row blocks of St
+// Global loads of the next slab / block go to registers before the current one is
+// computed.
+// ---------------------------------------------------------------------------
+constexpr int BT = 64;   // internal chunk length
+constexpr int KS = 16;   // slab width over dx
+constexpr int LP = 68;   // padded row length of the k-major tiles (16-byte aligned rows)
+
+template <typename TO> __device__ __forceinline__ void st4(TO* p, float4 v);
+template <> __device__ __forceinline__ void st4<float>(float* p, float4 v) {
+    *reinterpret_cast<float4*>(p) = v;
+}
+template <> __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+__device__ __forceinline__ float comp(const float4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(kThreads)
+chunkwise_backward_blocked_kernel(const ScanArgs args, int H, int N, const HeadConsts hc) {
+    extern __shared__ __align__(16) float smem[];
+    int ri = 0;
+    while (ri + 1 < args.nroles && (int)blockIdx.x >= args.role[ri + 1].cta0) ++ri;
+    const ScanRole& R = args.role[ri];
+    const int dx = R.dx, dz = R.dz;
+    const bool rev = R.rev != 0;
+    float* St = smem;                 // [dx][CS]   carried state slice
+    float* Zs = St + dx * CS;         // [BT][CS]   z rows of the chunk
+    float* Zw = Zs + BT * CS;         // [BT][CS]   the same rows times w_r
+    float* XT = Zw + BT * CS;         // [KS][LP]   x slab, k-major
+    float* YT = XT + KS * LP;         // [KS][LP]   y slab, k-major
+    float* PT = YT + KS * LP;         // [BT][LP]   decayed scores, key-major; then y block
+
+    const int local = blockIdx.x - R.cta0;
+    const int bh = local / R.slices;
+    const int c0 = (local % R.slices) * CS;
+    const int ncol = min(CS, dz - c0);
+    const int h = bh % H;
+    const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
+    const float l2g = hc.l2g[h];
+    const float gB = hc.gB[h];        // gamma^BT
+    const TI* xb = static_cast<const TI*>(R.x) + (size_t)bh * N * dx;
+    const TI* yb = static_cast<const TI*>(R.y) + (size_t)bh * N * dx;
+    const TI* zb = static_cast<const TI*>(R.z) + (size_t)bh * N * dz;
+    TO* ob = static_cast<TO*>(R.out) + (size_t)bh * N * dz;
+
+    for (int e = t; e < dx * CS; e += kThreads) {
+        const int a = e / CS, c = e % CS;
+        float s = 0.f;
+        if (R.st_in && c < ncol)
+            s = R.st_in_t ? R.st_in[((size_t)bh * dz + c0 + c) * dx + a]
+                          : R.st_in[((size_t)bh * dx + a) * dz + c0 + c];
+        St[e] = s;
+    }
+
+    const int nch = N / BT;
+    const int nslab = dx / KS;
+    const int nblk = (dx + BT - 1) / BT;
+    for (int ii = 0; ii < nch; ++ii) {
+        const int i0 = (rev ? nch - 1 - ii : ii) * BT;
+        const TI* xc = xb + (size_t)i0 * dx;
+        const TI* yc = yb + (size_t)i0 * dx;
+        // previous chunk's readers of Zs / Zw / St are done
+        __syncthreads();
+        for (int u = 0; u < (BT * CS) / kThreads; ++u) {
+            const int e = t + kThreads * u, r = e >> 6, c = e & 63;
+            const float zv = (c < ncol) ? ld(zb + (size_t)(i0 + r) * dz + c0 + c) : 0.f;
+            Zs[e] = zv;
+            Zw[e] = zv * decay_pow(l2g, (float)(rev ? r + 1 : BT - 1 - r));
+        }
+        float S[4][4], O[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S[i][j] = O[i][j] = 0.f;
+        // slab element u of this thread: row (t + 256u) / KS, column (t + 256u) % KS
+        float px[4], py[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = t + kThreads * u, r = e >> 4, k = e & 15;
+            px[u] = ld(xc + (size_t)r * dx + k);
+            py[u] = ld(yc + (size_t)r * dx + k);
+        }
+        for (int sl = 0; sl < nslab; ++sl) {
+            __syncthreads();   // readers of the previous slab are done
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = t + kThreads * u, r = e >> 4, k = e & 15;
+                XT[k * LP + r] = px[u];
+                YT[k * LP + r] = py[u];
+            }
+            __syncthreads();
+            if (sl + 1 < nslab) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = t + kThreads * u, r = e >> 4, k = e & 15;
+                    px[u] = ld(xc + (size_t)r * dx + (sl + 1) * KS + k);
+                    py[u] = ld(yc + (size_t)r * dx + (sl + 1) * KS + k);
+                }
+            }
+            const float* st_slab = St + (size_t)sl * KS * CS;
+#pragma unroll 4
+            for (int k = 0; k < KS; ++k) {
+                const float4 xa = *reinterpret_cast<const float4*>(XT + k * LP + 4 * ty);
+                const float4 yv = *reinterpret_cast<const float4*>(YT + k * LP + 4 * tx);
+                const float4 sv = *reinterpret_cast<const float4*>(st_slab + k * CS + 4 * tx);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float xi = comp(xa, i);
+                    S[i][0] = fmaf(xi, yv.x, S[i][0]); S[i][1] = fmaf(xi, yv.y, S[i][1]);
+                    S[i][2] = fmaf(xi, yv.z, S[i][2]); S[i][3] = fmaf(xi, yv.w, S[i][3]);
+                    O[i][0] = fmaf(xi, sv.x, O[i][0]); O[i][1] = fmaf(xi, sv.y, O[i][1]);
+                    O[i][2] = fmaf(xi, sv.z, O[i][2]); O[i][3] = fmaf(xi, sv.w, O[i][3]);
+                }
+            }
+        }
+        // decayed scores on the causal side, stored key-major
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int r = 4 * tx + jj;
+            float4 p;
+            float* pp = &p.x;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * ty + i;
+                const int ex = rev ? r - j : j - r;
+                pp[i] = ex >= 0 ? S[i][jj] * decay_pow(l2g, (float)ex) : 0.f;
+            }
+            *reinterpret_cast<float4*>(PT + r * LP + 4 * ty) = p;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = 4 * ty + i;
+            const float cf = decay_pow(l2g, (float)(rev ? BT - 1 - j : j + 1));
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) O[i][jj] *= cf;
+        }
+#pragma unroll 4
+        for (int r = 0; r < BT; ++r) {
+            const float4 pa = *reinterpret_cast<const float4*>(PT + r * LP + 4 * ty);
+            const float4 zv = *reinterpret_cast<const float4*>(Zs + r * CS + 4 * tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float pi = comp(pa, i);
+                O[i][0] = fmaf(pi, zv.x, O[i][0]); O[i][1] = fmaf(pi, zv.y, O[i][1]);
+                O[i][2] = fmaf(pi, zv.z, O[i][2]); O[i][3] = fmaf(pi, zv.w, O[i][3]);
+            }
+        }
+        if (4 * tx < ncol) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                st4<TO>(ob + (size_t)(i0 + 4 * ty + i) * dz + c0 + 4 * tx,
+                        make_float4(O[i][0], O[i][1], O[i][2], O[i][3]));
+        }
+        // carried state, 64 rows at a time: St = gamma^BT St + Y^T Zw
+        float py16[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int e = t + kThreads * u, r = e >> 6, al = e & 63;
+            py16[u] = (al < dx) ? ld(yc + (size_t)r * dx + al) : 0.f;
+        }
+        for (int ab = 0; ab < nblk; ++ab) {
+            __syncthreads();   // PT (scores, or the previous y block) is no longer read
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int e = t + kThreads * u, r = e >> 6, al = e & 63;
+                PT[r * LP + al] = py16[u];
+            }
+            __syncthreads();
+            if (ab + 1 < nblk) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int e = t + kThreads * u, r = e >> 6, al = e & 63;
+                    const int a = (ab + 1) * BT + al;
+                    py16[u] = (a < dx) ? ld(yc + (size_t)r * dx + a) : 0.f;
+                }
+            }
+            const int a0 = ab * BT + 4 * ty;
+            if (a0 < dx) {
+                float A[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) A[i][j] = 0.f;
+#pragma unroll 4
+                for (int r = 0; r < BT; ++r) {
+                    const float4 ya = *reinterpret_cast<const float4*>(PT + r * LP + 4 * ty);
+                    const float4 zv = *reinterpret_cast<const float4*>(Zw + r * CS + 4 * tx);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float yi = comp(ya, i);
+                        A[i][0] = fmaf(yi, zv.x, A[i][0]); A[i][1] = fmaf(yi, zv.y, A[i][1]);
+                        A[i][2] = fmaf(yi, zv.z, A[i][2]); A[i][3] = fmaf(yi, zv.w, A[i][3]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float4* sp = reinterpret_cast<float4*>(St + (size_t)(a0 + i) * CS + 4 * tx);
+                    float4 sv = *sp;
+                    sv.x = fmaf(gB, sv.x, A[i][0]); sv.y = fmaf(gB, sv.y, A[i][1]);
+                    sv.z = fmaf(gB, sv.z, A[i][2]); sv.w = fmaf(gB, sv.w, A[i][3]);
+                    *sp = sv;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (R.st_out) {
+        for (int e = t; e < dx * CS; e += kThreads) {
+            const int a = e / CS, c = e % CS;
+            if (c < ncol) R.st_out[((size_t)bh * dx + a) * dz + c0 + c] = St[e];
+        }
+    }
+}
+
 template <typename TI, typename TO>
 cudaError_t launch_bwd(ScanArgs& args, int bH, int H, int N, int chunk, const HeadConsts& hc,
                        cudaStream_t s) {
@@ -202,13 +435,22 @@ cudaError_t launch_bwd(ScanArgs& args, int bH, int H, int N, int chunk, const He
         if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         dxmax = r.dx > dxmax ? r.dx : dxmax;
     }
-    const size_t smem = sizeof(float) * ((size_t)dxmax * CS + 2 * (size_t)CT * (dxmax + 1) +
-                                         CT * CS + CT * (CT + 1));
-    auto kern = chunkwise_backward_simt_kernel<TI, TO>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(args, H, N, chunk, hc);
+    cudaError_t e;
+    if (chunk == BT) {   // register-blocked kernel (the caller passes BT when N % BT == 0)
+        const size_t smem = sizeof(float) * ((size_t)dxmax * CS + 2 * (size_t)BT * CS +
+                                             2 * (size_t)KS * LP + (size_t)BT * LP);
+        auto kern = chunkwise_backward_blocked_kernel<TI, TO>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, kThreads, smem, s>>>(args, H, N, hc);
+    } else {
+        const size_t smem = sizeof(float) * ((size_t)dxmax * CS + 2 * (size_t)CT * (dxmax + 1) +
+                                             CT * CS + CT * (CT + 1));
+        auto kern = chunkwise_backward_simt_kernel<TI, TO>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, kThreads, smem, s>>>(args, H, N, chunk, hc);
+    }
     cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_BACKWARD_SIMT);
     return err;

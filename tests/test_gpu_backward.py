@@ -50,8 +50,12 @@ def run(q, k, v, do, gamma, chunk, s0=None, ds=None, out_dtype=torch.float32):
     return gq, gk, gv, di
 
 
+# N a multiple of 64 takes the register-blocked kernel (64-token chunks whatever the
+# chunk argument); other N the 16-row kernel with the caller's chunk.
 @pytest.mark.parametrize("b,H,N,dk,dv,chunk", [(1, 2, 128, 64, 128, 32), (2, 3, 256, 48, 80, 64),
-                                               (1, 2, 96, 256, 512, 16), (1, 1, 512, 128, 64, 256)])
+                                               (1, 2, 96, 256, 512, 16), (1, 1, 512, 128, 64, 256),
+                                               (1, 2, 80, 64, 48, 16), (2, 1, 160, 32, 96, 32),
+                                               (1, 1, 192, 256, 512, 48)])
 def test_fp32_parity(b, H, N, dk, dv, chunk):
     gamma = [0.97, 0.6, 0.999][:H]
     q, k, v, do, s0, ds = make(b, H, N, dk, dv, 100 + dk + dv + chunk)
@@ -97,14 +101,16 @@ def test_no_states_and_extreme_decays():
         assert err_f32(g, w) < TOL_F32, name
 
 
-def test_chunk_length_does_not_change_the_gradient():
-    b, H, N, dk, dv = 1, 2, 256, 64, 128
-    q, k, v, do, s0, ds = make(b, H, N, dk, dv, 600)
-    ref = run(q, k, v, do, [0.95, 0.8], 16, s0, ds)
-    for chunk in (32, 128, 256):
-        got = run(q, k, v, do, [0.95, 0.8], chunk, s0, ds)
-        for g, r in zip(got, ref):
-            assert err_f32(g, r) < 1e-5
+def test_both_kernels_agree_on_the_causal_prefix():
+    """dq_n depends on tokens m <= n only, so dq of a 192-token sequence (register-blocked
+    kernel, 64-token chunks) equals the first 192 rows of dq of the same sequence extended
+    to 208 tokens (16-row kernel, chunk 16)."""
+    b, H, dk, dv = 1, 2, 64, 128
+    q, k, v, do, s0, _ = make(b, H, 208, dk, dv, 600)
+    short = [t[:, :, :192].contiguous() for t in (q, k, v, do)]
+    dq_long = run(q, k, v, do, [0.95, 0.8], 16, s0)[0]
+    dq_short = run(*short, [0.95, 0.8], 16, s0)[0]
+    assert err_f32(dq_short, dq_long[:, :, :192]) < 1e-5
 
 
 def test_empty_sequence_passes_the_state_gradient_through():
