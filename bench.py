@@ -394,7 +394,9 @@ def bench_backward(args, dist, rb, pk):
                         "dq/dk/dv (retention_chunkwise_backward, CUDA-core kernel)",
             "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": profile_traffic("chunkwise_backward_blocked_backward.md",
+                                                    "simt_backward.cu"),
                          "algorithmic_flops_per_launch": flops,
                          "peak_basis": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x max SM clock"}}
 
