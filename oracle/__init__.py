@@ -83,9 +83,10 @@ class Oracle:
         lib.oracle_brute.argtypes = [P, P, P, P, I, I, I, I, I, P]
         lib.oracle_msr_epilogue.argtypes = [P, P, P, I, I, I, I, ctypes.c_double, P, P]
         lib.oracle_chunkwise_backward.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, P]
+        lib.oracle_rglru.argtypes = [P, P, P, P, P, P, P, I, I, I, ctypes.c_double]
         for f in ("oracle_parallel", "oracle_recurrent", "oracle_recurrent_step",
                   "oracle_chunkwise", "oracle_brute", "oracle_msr_epilogue",
-                  "oracle_chunkwise_backward"):
+                  "oracle_chunkwise_backward", "oracle_rglru"):
             getattr(lib, f).restype = ctypes.c_int
         self.lib = lib
 
@@ -158,6 +159,18 @@ class Oracle:
                                                   dv, _p(g)), "chunkwise_backward")
         return gq, gk, gv, gs
 
+    def rglru(self, x, gate_a, gate_x, lambda_, h0=None, c: float = 8.0,
+              return_state: bool = False):
+        """RG-LRU scan (Griffin page); x, gate_a, gate_x: [b,T,D], lambda_: [D], h0: [b,D]."""
+        x, ga, gx, lam = _f64(x), _f64(gate_a), _f64(gate_x), _f64(lambda_)
+        b, T, D = x.shape
+        h0 = _f64(h0)
+        y = np.zeros((b, T, D))
+        hl = np.zeros((b, D))
+        _check(self.lib.oracle_rglru(_p(x), _p(ga), _p(gx), _p(lam), _p(h0), _p(y), _p(hl),
+                                     b, T, D, float(c)), "rglru")
+        return (y, hl) if return_state else y
+
     def msr_epilogue(self, y, g, eps: float, weight=None, bias=None) -> np.ndarray:
         """GroupNorm per (token, head) then swish(G) gate; y:[b,H,N,dv] g:[b,N,H*dv]."""
         y, g = _f64(y), _f64(g)
@@ -203,6 +216,10 @@ def msr_epilogue(*a, **kw):
 
 def chunkwise_backward(*a, **kw):
     return default().chunkwise_backward(*a, **kw)
+
+
+def rglru(*a, **kw):
+    return default().rglru(*a, **kw)
 
 
 def map_units(fn, units, threads: int | None = None):

@@ -398,3 +398,41 @@ int oracle_chunkwise_backward(const double* q, const double* k, const double* v,
         }
     return 0;
 }
+
+/*
+ * RG-LRU scan of the Griffin page ("Griffin ：將門控線性循環與局部注意力混合以實現
+ * 高效的語言模型", section "實門線性循環單元 (RG-LRU)", its four equations), a second
+ * linear recurrence.  Per batch row, channel d and step t, from the gate
+ * pre-activations (the two projections W_a x_t + b_a and W_x x_t + b_x are plain
+ * matrix products outside this step):
+ *   r_t = sigmoid(gate_a_t)             recurrence gate
+ *   i_t = sigmoid(gate_x_t)             input gate
+ *   a   = sigmoid(lambda_d)             so 0 <= a <= 1
+ *   a_t = a^(c r_t)                     (the page fixes c = 8)
+ *   h_t = a_t h_{t-1} + sqrt(1 - a_t^2) (i_t x_t),   y_t = h_t
+ * with h_{-1} = h0 (NULL means zero).  Written as the definition, with pow; the page
+ * evaluates a_t in log space, which is the same number.
+ * x, gate_a, gate_x, y: [b][T][D]; lambda: [D]; h0, h_last: [b][D] (h_last nullable).
+ */
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+int oracle_rglru(const double* x, const double* gate_a, const double* gate_x,
+                 const double* lambda_, const double* h0, double* y, double* h_last,
+                 int b, int T, int D, double c) {
+    if (b < 0 || T < 0 || D <= 0 || !(c >= 0.0)) return -1;
+    for (int bi = 0; bi < b; ++bi)
+        for (int d = 0; d < D; ++d) {
+            double h = h0 ? h0[(size_t)bi * D + d] : 0.0;
+            double a = sigmoid(lambda_[d]);
+            for (int t = 0; t < T; ++t) {
+                size_t e = ((size_t)bi * T + t) * D + d;
+                double r = sigmoid(gate_a[e]);
+                double i = sigmoid(gate_x[e]);
+                double at = pow(a, c * r);
+                h = at * h + sqrt(1.0 - at * at) * (i * x[e]);
+                y[e] = h;
+            }
+            if (h_last) h_last[(size_t)bi * D + d] = h;
+        }
+    return 0;
+}
