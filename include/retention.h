@@ -232,6 +232,26 @@ int retention_parallel_gated(const void* q, const void* k, const void* v, const 
                              const double* gamma, unsigned flags, float eps,
                              const float* weight, const float* bias, void* stream);
 
+/*
+ * RG-LRU scan, the gated diagonal linear recurrence of the Griffin page ("Griffin ：
+ * 將門控線性循環與局部注意力混合以實現高效的語言模型", section "實門線性循環單元
+ * (RG-LRU)"), from the pre-activations of its two gates (the projections
+ * W_a x_t + b_a and W_x x_t + b_x are plain matrix products, not part of this call):
+ *   r_t = sigmoid(gate_a_t), i_t = sigmoid(gate_x_t), a = sigmoid(lambda[d]),
+ *   a_t = a^(c r_t),  h_t = a_t h_{t-1} + sqrt(1 - a_t^2) (i_t x_t),  y_t = h_t,
+ * elementwise over the D channels, sequential over t, h_{-1} = h0 (NULL means zero);
+ * a_t is evaluated in log space.  The page fixes c = 8.
+ * x, gate_a, gate_x: [b][T][D] in in_dtype; y: [b][T][D] in out_dtype (written, must
+ * not overlap the inputs); lambda: [D] fp32; h0, h_last: [b][D] fp32, nullable
+ * (h_last receives h_{T-1}, or h0 when T = 0).  All DEVICE pointers, 16-byte aligned.
+ * D must be a multiple of 8 (RET_ERR_UNSUPPORTED), c finite and >= 0
+ * (RET_ERR_UNSUPPORTED); negative sizes return RET_ERR_SHAPE; b, T or D of zero launch
+ * nothing (T = 0 still writes h_last).  One memory-bound kernel launch.
+ */
+int rglru_scan(const void* x, const void* gate_a, const void* gate_x, const float* lambda_,
+               const float* h0, void* y, float* h_last, ret_dtype in_dtype,
+               ret_dtype out_dtype, int b, int T, int D, float c, void* stream);
+
 /* Static text for a ret_status code ("unknown status" for other values). */
 const char* retention_status_string(int status);
 
@@ -271,7 +291,8 @@ enum {
     RET_KERNEL_PARALLEL_TC = 6,     /* parallel form, tcgen05 tensor-core kernel      */
     RET_KERNEL_PARALLEL_GATED_TC = 7, /* parallel form + gated GroupNorm, tensor cores */
     RET_KERNEL_CHUNKWISE_TC_PAIR = 8, /* chunkwise form, tensor cores on pairs of SMs */
-    RET_KERNEL_CHUNKWISE_BACKWARD_SIMT = 9 /* chunkwise gradient, CUDA-core fp32 FMA    */
+    RET_KERNEL_CHUNKWISE_BACKWARD_SIMT = 9, /* chunkwise gradient, CUDA-core fp32 FMA   */
+    RET_KERNEL_RGLRU = 10           /* RG-LRU scan                                    */
 };
 
 /*

@@ -25,7 +25,7 @@ NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
                 5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair",
-                9: "chunkwise_backward_simt"}
+                9: "chunkwise_backward_simt", 10: "rglru"}
 
 _lib = None
 _lock = threading.Lock()
@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             L.retention_chunkwise.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp, vp, vp, vp]
             L.retention_chunkwise_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                                        i, i, i, dp, vp, vp, vp, vp]
+            L.rglru_scan.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
             L.retention_recurrent_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, dp, vp]
             L.msr_epilogue.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, vp]
             L.retention_parallel_gated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp,
@@ -200,6 +201,25 @@ def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None
         _ptr(state_in), _ptr(dstate_out), _ptr(dstate_in), _stream(stream))
     _check("retention_chunkwise_backward", rc)
     return gq, gk, gv, dstate_in
+
+
+def rglru_scan(x, gate_a, gate_x, lambda_, h0=None, c: float = 8.0, out=None,
+               out_dtype=torch.float32, h_last=None, stream=None):
+    """RG-LRU scan (Griffin page).  x, gate_a, gate_x: [b,T,D]; lambda_: fp32 [D];
+    h0, h_last: fp32 [b,D] or None.  Returns y [b,T,D]."""
+    b, T, D = x.shape
+    if gate_a.dtype != x.dtype or gate_x.dtype != x.dtype:
+        raise TypeError("x, gate_a and gate_x must share one dtype")
+    for s in (lambda_, h0, h_last):
+        if s is not None and s.dtype != torch.float32:
+            raise TypeError("lambda, h0 and h_last are fp32")
+    if out is None:
+        out = torch.empty((b, T, D), dtype=out_dtype, device=x.device)
+    rc = lib().rglru_scan(_ptr(x), _ptr(gate_a), _ptr(gate_x), _ptr(lambda_), _ptr(h0),
+                          _ptr(out), _ptr(h_last), _dtype_code(x.dtype), _dtype_code(out.dtype),
+                          b, T, D, ctypes.c_float(c), _stream(stream))
+    _check("rglru_scan", rc)
+    return out
 
 
 _copy_streams = {}

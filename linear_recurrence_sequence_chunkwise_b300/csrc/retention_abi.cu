@@ -251,6 +251,35 @@ int msr_epilogue(const void* y, const void* g, void* out, ret_dtype y_dtype, ret
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+int rglru_scan(const void* x, const void* gate_a, const void* gate_x, const float* lambda_,
+               const float* h0, void* y, float* h_last, ret_dtype in_dtype,
+               ret_dtype out_dtype, int b, int T, int D, float c, void* stream) {
+    if (b < 0 || T < 0 || D < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (D % 8 != 0) return RET_ERR_UNSUPPORTED;
+    if (!(c >= 0.0f) || isinf(c)) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || D == 0) return RET_OK;
+    if ((h0 && !aligned16(h0)) || (h_last && !aligned16(h_last))) return RET_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // No steps: the final state is the incoming one.
+        if (!h_last) return RET_OK;
+        size_t bytes = (size_t)b * D * sizeof(float);
+        if (h0) {
+            if (h0 == h_last) return RET_OK;
+            return cuda_status(cudaMemcpyAsync(h_last, h0, bytes, cudaMemcpyDeviceToDevice, s));
+        }
+        return cuda_status(cudaMemsetAsync(h_last, 0, bytes, s));
+    }
+    if (!x || !gate_a || !gate_x || !lambda_ || !y) return RET_ERR_NULL;
+    if (!aligned16(x) || !aligned16(gate_a) || !aligned16(gate_x) || !aligned16(lambda_) ||
+        !aligned16(y))
+        return RET_ERR_ALIGN;
+    return cuda_status(ret::launch_rglru_scan(x, gate_a, gate_x, lambda_, h0, y, h_last,
+                                              in_dtype == RET_BF16, out_dtype == RET_BF16, b,
+                                              T, D, c, s));
+}
+
 unsigned long long retention_kernel_launches(void) { return ret::g_launches.load(); }
 
 int retention_last_kernel(void) { return ret::t_last_kernel; }

@@ -15,6 +15,8 @@ synthetic):
   decode          b128 H16 dk256 dv512, state N(0, sigma=0.1), 512 steps of
                   bf16 q,k,v ~ N(0,1)/sqrt(dk)
   backward        b4  H16 dk256 dv512 N2048   chunk 64   bf16 q,k,v,dout N(0,1)/sqrt(dk)
+  rglru           b8  T4096 D4096 (RG-LRU scan)          bf16 x, gate pre-activations N(0,1),
+                  Lambda with a^8 ~ U(0.9, 0.999)
 Decay schedule: gamma_h = 1 - 2^(-5-h) (one fixed decay per head, as the
 multi-scale retention section prescribes; the schedule itself is a choice).
 """
@@ -71,7 +73,14 @@ DECODE = Workload("decode", 128, 16, 1, 256, 512, "bf16", 1.0 / 16.0, steps=512,
 # gradient of the chunkwise form at the first training-sweep shape; dout ~ N(0,1)/sqrt(dk)
 BACKWARD = Workload("backward", 4, 16, 2048, 256, 512, "bf16", 1.0 / 16.0, chunk=64, seed=6000)
 
-WORKLOADS = {w.name: w for w in [TINY, PARALLEL_NORM, CHUNKWISE_LONG, DECODE, BACKWARD] + SWEEP}
+# RG-LRU scan (Griffin page): b rows, T steps, D channels; x and the two gate
+# pre-activations N(0,1) bf16, Lambda drawn so that a^c is uniform in [0.9, 0.999] (the
+# page's initialisation), zero initial state, fp32 output.  Workload fields: N = T,
+# dv = D (dk unused).
+RGLRU = Workload("rglru", 8, 1, 4096, 0, 4096, "bf16", 1.0, seed=7000)
+
+WORKLOADS = {w.name: w for w in [TINY, PARALLEL_NORM, CHUNKWISE_LONG, DECODE, BACKWARD,
+                                 RGLRU] + SWEEP}
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -116,6 +125,24 @@ def dout(w: Workload, device="cpu", N: int | None = None) -> torch.Tensor:
     """Upstream gradient of the output, [b,H,N,dv] in the storage dtype."""
     N = w.N if N is None else N
     return randn((w.b, w.H, N, w.dv), w.seed + 7, w.scale, w.dtype, device)
+
+
+def rglru_lambda(D: int, seed: int, c: float = 8.0, device="cpu") -> torch.Tensor:
+    """Lambda [D] fp32 with a^c ~ U(0.9, 0.999) for a = sigmoid(Lambda), the Griffin page's
+    initialisation: a = u^(1/c), Lambda = log(a / (1 - a)) (computed in fp64)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.uniform(0.9, 0.999, size=D) ** (1.0 / c)
+    return torch.from_numpy(np.log(a / (1.0 - a))).to(torch.float32).to(device)
+
+
+def rglru_inputs(w: Workload, device="cpu", T: int | None = None):
+    """x, gate_a, gate_x [b,T,D] in the storage dtype and Lambda [D] fp32."""
+    T = w.N if T is None else T
+    shape = (w.b, T, w.dv)
+    x = randn(shape, w.seed + 1, w.scale, w.dtype, device)
+    ga = randn(shape, w.seed + 2, 1.0, w.dtype, device)
+    gx = randn(shape, w.seed + 3, 1.0, w.dtype, device)
+    return x, ga, gx, rglru_lambda(w.dv, w.seed + 4, 8.0, device)
 
 
 def gate(w: Workload, device="cpu", N: int | None = None) -> torch.Tensor:

@@ -38,7 +38,7 @@ def test_exports_every_declared_function(L):
                           "retention_chunkwise_host", "retention_chunkwise_host_workspace_bytes",
                           "retention_chunkwise_host_noalloc",
                           "retention_chunkwise_host_static_scratch_bytes",
-                          "retention_chunkwise_backward"}
+                          "retention_chunkwise_backward", "rglru_scan"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
@@ -157,6 +157,29 @@ def test_chunkwise_backward_rejections(L):
     # empty inputs: nothing to compute (no dstate_in requested)
     assert bwd(L, b=0, q=NUL, k=NUL, v=NUL, do=NUL, gq=NUL, gk=NUL, gv=NUL) == binding.RET_OK
     assert bwd(L, N=0, q=NUL, k=NUL, v=NUL, do=NUL, gq=NUL, gk=NUL, gv=NUL) == binding.RET_OK
+    assert binding.kernel_launches() == before
+
+
+def rg(L, x=A, ga=A, gx=A, lam=A, h0=None, y=A2, hl=None, it=1, ot=0, b=2, T=64, D=64, c=8.0):
+    return L.rglru_scan(x, ga, gx, lam, h0, y, hl, it, ot, b, T, D, ctypes.c_float(c), S)
+
+
+def test_rglru_rejections(L):
+    before = binding.kernel_launches()
+    assert rg(L, b=-1) == binding.RET_ERR_SHAPE
+    assert rg(L, T=-1) == binding.RET_ERR_SHAPE
+    assert rg(L, it=2) == binding.RET_ERR_DTYPE
+    assert rg(L, D=12) == binding.RET_ERR_UNSUPPORTED
+    assert rg(L, c=-1.0) == binding.RET_ERR_UNSUPPORTED
+    assert rg(L, c=float("inf")) == binding.RET_ERR_UNSUPPORTED
+    assert rg(L, c=float("nan")) == binding.RET_ERR_UNSUPPORTED
+    assert rg(L, x=NUL) == binding.RET_ERR_NULL
+    assert rg(L, lam=NUL) == binding.RET_ERR_NULL
+    assert rg(L, gx=MIS) == binding.RET_ERR_ALIGN
+    assert rg(L, h0=MIS) == binding.RET_ERR_ALIGN
+    assert rg(L, hl=MIS) == binding.RET_ERR_ALIGN
+    assert rg(L, b=0, x=NUL, ga=NUL, gx=NUL, lam=NUL, y=NUL) == binding.RET_OK
+    assert rg(L, T=0, x=NUL, ga=NUL, gx=NUL, lam=NUL, y=NUL) == binding.RET_OK
     assert binding.kernel_launches() == before
 
 
