@@ -244,9 +244,11 @@ int retention_parallel_gated(const void* q, const void* k, const void* v, const 
  * x, gate_a, gate_x: [b][T][D] in in_dtype; y: [b][T][D] in out_dtype (written, must
  * not overlap the inputs); lambda: [D] fp32; h0, h_last: [b][D] fp32, nullable
  * (h_last receives h_{T-1}, or h0 when T = 0).  All DEVICE pointers, 16-byte aligned.
- * D must be a multiple of 8 (RET_ERR_UNSUPPORTED), c finite and >= 0
+ * D must be a multiple of 64 (RET_ERR_UNSUPPORTED), c finite and >= 0
  * (RET_ERR_UNSUPPORTED); negative sizes return RET_ERR_SHAPE; b, T or D of zero launch
- * nothing (T = 0 still writes h_last).  One memory-bound kernel launch.
+ * nothing (T = 0 still writes h_last).  One memory-bound kernel launch: each CTA owns
+ * 64 channels; its warps scan consecutive segments of t from a zero state and combine
+ * them with the (prod a_t, h_end) pairs of the segments before them.
  */
 int rglru_scan(const void* x, const void* gate_a, const void* gate_x, const float* lambda_,
                const float* h0, void* y, float* h_last, ret_dtype in_dtype,

@@ -256,7 +256,7 @@ int rglru_scan(const void* x, const void* gate_a, const void* gate_x, const floa
                ret_dtype out_dtype, int b, int T, int D, float c, void* stream) {
     if (b < 0 || T < 0 || D < 0) return RET_ERR_SHAPE;
     if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
-    if (D % 8 != 0) return RET_ERR_UNSUPPORTED;
+    if (D % 64 != 0) return RET_ERR_UNSUPPORTED;
     if (!(c >= 0.0f) || isinf(c)) return RET_ERR_UNSUPPORTED;
     if (b == 0 || D == 0) return RET_OK;
     if ((h0 && !aligned16(h0)) || (h_last && !aligned16(h_last))) return RET_ERR_ALIGN;

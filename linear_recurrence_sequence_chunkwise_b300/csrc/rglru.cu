@@ -7,18 +7,22 @@
 // in log space, as the page prescribes: log2 a_t = c r_t log2 sigmoid(lambda), and
 // 1 - a_t^2 = -expm1(2 ln a_t), so that a_t close to 1 keeps its precision.
 //
-// Memory-bound: per step and channel three inputs are read and one output written.
-// One thread owns two adjacent channels of one batch row (8-byte or 4-byte vector
-// accesses, a warp covers 64 consecutive channels) and scans t in blocks of P steps;
-// the loads of block k+1 are issued into registers before block k is computed, so
-// P steps of three inputs per thread are in flight while the recurrence runs.
+// Memory-bound: per step and channel three inputs are read and one output written,
+// each exactly once.  The sequential dependence on t is split the chunkwise way:
+// a CTA owns 64 channels of one batch row (a warp lane owns two adjacent ones) and
+// walks t in tiles of 8 segments; warp w scans segment w of the tile from a zero state,
+// keeping each step's local output y_loc and decay product P (= prod of a_s since the
+// segment start) in registers, and publishes the segment's (prod a, h_end) through
+// shared memory.  Each warp then folds the published pairs of the segments before its
+// own into the state entering its segment, c, and writes y_t = y_loc_t + P_t c.  The
+// last warp carries the tile's final state to the next tile.  A warp loads its whole
+// segment (3 x SEG rows of 128 or 256 contiguous bytes) before computing it.
 #include "common.cuh"
 
 namespace ret {
 namespace {
 
-// Small blocks: b * D / 2 threads in all (16 K for 8 x 4096 channels) spread over every SM.
-constexpr int kThreads = 64;
+constexpr int kThreads = 256;
 
 template <typename T> struct Vec2;
 template <> struct Vec2<float> {
@@ -56,82 +60,94 @@ __device__ __forceinline__ float one_minus_exp(float u) {
     return 1.0f - __expf(u);
 }
 
-// One step for one channel; la2 = log2 sigmoid(lambda).
+// One step for one channel; la2 = log2 sigmoid(lambda).  Returns h_t, and a_t in at.
 __device__ __forceinline__ float rglru_step(float h, float x, float ga, float gx, float la2,
-                                            float c) {
+                                            float c, float& at) {
     const float r = sigmoidf_(ga);
     const float l2 = (r > 0.0f) ? c * r * la2 : 0.0f;        // log2 a_t (a^0 = 1, also for a = 0)
-    const float at = exp2f(l2);
+    at = exp2f(l2);
     const float w = sqrtf(one_minus_exp(2.0f * 0.69314718055994531f * l2));
     return fmaf(at, h, w * (sigmoidf_(gx) * x));
 }
 
-template <typename TI, typename TO, int P>
-__global__ void __launch_bounds__(kThreads)
+constexpr int kWarps = 8;        // segments per tile
+constexpr int kLanes = 32;       // a lane owns channels 2*lane, 2*lane+1 of the CTA's 64
+
+template <typename TI, typename TO, int SEG>
+__global__ void __launch_bounds__(kThreads, 2)
 rglru_scan_kernel(const TI* __restrict__ x, const TI* __restrict__ ga, const TI* __restrict__ gx,
                   const float* __restrict__ lam, const float* __restrict__ h0,
                   TO* __restrict__ y, float* __restrict__ h_last, int b, int T, int D, float c) {
     using V = typename Vec2<TI>::type;
-    const int pairs = D >> 1;
-    const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
-    if (idx >= (long long)b * pairs) return;
-    const int bi = (int)(idx / pairs);
-    const int d = (int)(idx % pairs) * 2;
+    __shared__ float2 segA[kWarps][kLanes];   // prod of a_t over the segment, per channel
+    __shared__ float2 segH[kWarps][kLanes];   // segment's final state from a zero start
+    __shared__ float2 carry[kLanes];          // state entering the current tile
+    const int blocks_per_row = D / (2 * kLanes);
+    const int bi = blockIdx.x / blocks_per_row;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int d = (blockIdx.x % blocks_per_row) * (2 * kLanes) + 2 * lane;
     // log2 sigmoid(lambda) = -log2(1 + e^-lambda): -inf for a = 0, 0 for a = 1
     const float la0 = -log1pf(expf(-lam[d])) * 1.4426950408889634f;
     const float la1 = -log1pf(expf(-lam[d + 1])) * 1.4426950408889634f;
-    float h_0 = 0.f, h_1 = 0.f;
-    if (h0) {
-        h_0 = h0[(size_t)bi * D + d];
-        h_1 = h0[(size_t)bi * D + d + 1];
+    if (w == 0) {
+        float2 s0 = make_float2(0.f, 0.f);
+        if (h0) s0 = make_float2(h0[(size_t)bi * D + d], h0[(size_t)bi * D + d + 1]);
+        carry[lane] = s0;
     }
     const size_t base = (size_t)bi * T * D + d;
     const TI* xp = x + base;
     const TI* ap = ga + base;
     const TI* gp = gx + base;
     TO* yp = y + base;
-
-    V bx[P], ba[P], bg[P];
+    for (int t0 = 0; t0 < T; t0 += kWarps * SEG) {
+        const int ts = t0 + w * SEG;          // this warp's segment
+        V bx[SEG], ba[SEG], bg[SEG];
 #pragma unroll
-    for (int u = 0; u < P; ++u) {
-        if (u < T) {
-            bx[u] = Vec2<TI>::load(xp + (size_t)u * D);
-            ba[u] = Vec2<TI>::load(ap + (size_t)u * D);
-            bg[u] = Vec2<TI>::load(gp + (size_t)u * D);
-        }
-    }
-    for (int t0 = 0; t0 < T; t0 += P) {
-        V nx[P], na[P], ng[P];
-        const int tn = t0 + P;
-#pragma unroll
-        for (int u = 0; u < P; ++u) {
-            if (tn + u < T) {
-                nx[u] = Vec2<TI>::load(xp + (size_t)(tn + u) * D);
-                na[u] = Vec2<TI>::load(ap + (size_t)(tn + u) * D);
-                ng[u] = Vec2<TI>::load(gp + (size_t)(tn + u) * D);
+        for (int u = 0; u < SEG; ++u) {
+            if (ts + u < T) {
+                bx[u] = Vec2<TI>::load(xp + (size_t)(ts + u) * D);
+                ba[u] = Vec2<TI>::load(ap + (size_t)(ts + u) * D);
+                bg[u] = Vec2<TI>::load(gp + (size_t)(ts + u) * D);
             }
         }
+        float yl0[SEG], yl1[SEG], p0[SEG], p1[SEG];
+        float hl0 = 0.f, hl1 = 0.f, pa0 = 1.f, pa1 = 1.f;
 #pragma unroll
-        for (int u = 0; u < P; ++u) {
-            if (t0 + u < T) {
+        for (int u = 0; u < SEG; ++u) {
+            if (ts + u < T) {
                 const float2 xv = Vec2<TI>::unpack(bx[u]);
                 const float2 av = Vec2<TI>::unpack(ba[u]);
                 const float2 gv = Vec2<TI>::unpack(bg[u]);
-                h_0 = rglru_step(h_0, xv.x, av.x, gv.x, la0, c);
-                h_1 = rglru_step(h_1, xv.y, av.y, gv.y, la1, c);
-                store2(yp + (size_t)(t0 + u) * D, h_0, h_1);
+                float at;
+                hl0 = rglru_step(hl0, xv.x, av.x, gv.x, la0, c, at);
+                pa0 *= at;
+                hl1 = rglru_step(hl1, xv.y, av.y, gv.y, la1, c, at);
+                pa1 *= at;
             }
+            yl0[u] = hl0; yl1[u] = hl1; p0[u] = pa0; p1[u] = pa1;
         }
+        segA[w][lane] = make_float2(pa0, pa1);
+        segH[w][lane] = make_float2(hl0, hl1);
+        __syncthreads();
+        float2 cs = carry[lane];              // state entering the tile
+        for (int k = 0; k < w; ++k) {         // ... then entering this warp's segment
+            const float2 A = segA[k][lane], Hk = segH[k][lane];
+            cs.x = fmaf(A.x, cs.x, Hk.x);
+            cs.y = fmaf(A.y, cs.y, Hk.y);
+        }
+        __syncthreads();                      // every warp has read carry and the pairs
+        if (w == kWarps - 1)
+            carry[lane] = make_float2(fmaf(pa0, cs.x, hl0), fmaf(pa1, cs.y, hl1));
 #pragma unroll
-        for (int u = 0; u < P; ++u) {
-            bx[u] = nx[u];
-            ba[u] = na[u];
-            bg[u] = ng[u];
-        }
+        for (int u = 0; u < SEG; ++u)
+            if (ts + u < T)
+                store2(yp + (size_t)(ts + u) * D, fmaf(p0[u], cs.x, yl0[u]),
+                       fmaf(p1[u], cs.y, yl1[u]));
     }
-    if (h_last) {
-        h_last[(size_t)bi * D + d] = h_0;
-        h_last[(size_t)bi * D + d + 1] = h_1;
+    __syncthreads();
+    if (h_last && w == 0) {
+        h_last[(size_t)bi * D + d] = carry[lane].x;
+        h_last[(size_t)bi * D + d + 1] = carry[lane].y;
     }
 }
 
@@ -139,12 +155,12 @@ template <typename TI, typename TO>
 cudaError_t launch_rg(const void* x, const void* ga, const void* gx, const float* lam,
                       const float* h0, void* y, float* h_last, int b, int T, int D, float c,
                       cudaStream_t s) {
-    const long long threads = (long long)b * (D / 2);
-    const long long blocks = (threads + kThreads - 1) / kThreads;
+    // D % 64 == 0 is checked by the caller; one CTA per (batch row, 64 channels)
+    const long long blocks = (long long)b * (D / (2 * kLanes));
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // 16 steps in flight for 2-byte inputs, 8 for 4-byte ones (the same bytes)
-    constexpr int P = sizeof(TI) == 2 ? 16 : 8;
-    rglru_scan_kernel<TI, TO, P><<<(unsigned)blocks, kThreads, 0, s>>>(
+    // 16 steps per segment for 2-byte inputs, 8 for 4-byte ones (the same bytes)
+    constexpr int SEG = sizeof(TI) == 2 ? 16 : 8;
+    rglru_scan_kernel<TI, TO, SEG><<<(unsigned)blocks, kThreads, 0, s>>>(
         static_cast<const TI*>(x), static_cast<const TI*>(ga), static_cast<const TI*>(gx), lam,
         h0, static_cast<TO*>(y), h_last, b, T, D, c);
     cudaError_t err = cudaGetLastError();

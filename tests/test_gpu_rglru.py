@@ -1,7 +1,7 @@
 """rglru_scan (RG-LRU of the Griffin page) against the oracle.
 
 fp32 inputs at the 1e-4 relative metric, bf16 inputs at 2e-2 of the RMS; T not a
-multiple of the kernel's prefetch block, D a multiple of 8 but not of 64, the
+multiple of the kernel's segment or tile, several 64-channel blocks per row, the
 incoming and final states, gates driven to their limits, and the full-size workload
 (b8 T4096 D4096) on sampled channels.
 """
@@ -34,7 +34,8 @@ def make(b, T, D, seed, dtype="f32"):
     return x, ga, gx, lam, h0
 
 
-@pytest.mark.parametrize("b,T,D", [(2, 100, 24), (1, 257, 136), (3, 16, 8), (2, 1, 64)])
+@pytest.mark.parametrize("b,T,D", [(2, 100, 64), (1, 257, 192), (3, 16, 64), (2, 1, 128),
+                                   (1, 1000, 64)])
 def test_fp32_parity(b, T, D):
     x, ga, gx, lam, h0 = make(b, T, D, 100 + T + D)
     hl = torch.full((b, D), float("nan"), device=DEV)
@@ -60,7 +61,7 @@ def test_bf16_parity_and_bf16_output():
 def test_gate_limits_and_other_c():
     """Recurrence gate closed (r = 0: h stays h0), decay a = 0 (h = i x), a = 1, and
     c = 1 and 3.5 besides the page's 8."""
-    b, T, D = 2, 40, 32
+    b, T, D = 2, 40, 64
     x, ga, gx, lam, h0 = make(b, T, D, 300)
     ga[:, :, :8] = -1e4
     lam[8:16] = -1e4
@@ -73,7 +74,7 @@ def test_gate_limits_and_other_c():
 
 
 def test_empty_sequence_copies_the_state():
-    b, D = 2, 16
+    b, D = 2, 64
     e = torch.empty((b, 0, D), device=DEV)
     lam = torch.zeros(D, device=DEV)
     h0 = inputs.randn((b, D), 400, 1.0, "f32", DEV)
