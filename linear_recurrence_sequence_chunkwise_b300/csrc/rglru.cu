@@ -49,31 +49,59 @@ __device__ __forceinline__ void store2(__nv_bfloat16* p, float a, float b) {
     __stcs(reinterpret_cast<__nv_bfloat162*>(p), __floats2bfloat162_rn(a, b));
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) {
-    return __frcp_rn(1.0f + __expf(-z));   // IEEE reciprocal: z -> -inf gives exactly 0
+// Two arithmetic variants.  Accurate (fp32 inputs, 1e-4 relative tolerance): IEEE
+// reciprocal and square root, exp2f.  Fast (bf16 inputs): one hardware instruction each
+// for tanh, 2^x and the square root; sigmoid(z) = 1/2 + tanh(z/2)/2, whose error (below
+// 2.5e-4 absolute) sits far under the bf16 inputs' own rounding.  Both give exactly 0
+// for a gate driven to -inf (tanh saturates at -1, 1/inf = 0).
+__device__ __forceinline__ float tanh_hw(float v) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float ex2_hw(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float sqrt_hw(float v) {
+    float r;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
 }
 
-// 1 - e^u for u <= 0: the Taylor series -(u + u^2/2 + u^3/6 + u^4/24) where |u| is
-// small (its next term is below 2^-24 relative for |u| < 1/16), else 1 - e^u directly.
-__device__ __forceinline__ float one_minus_exp(float u) {
+template <bool FAST> __device__ __forceinline__ float sigm(float z) {
+    if (FAST) return fmaf(0.5f, tanh_hw(0.5f * z), 0.5f);
+    return __frcp_rn(1.0f + __expf(-z));
+}
+template <bool FAST> __device__ __forceinline__ float pow2(float v) {
+    return FAST ? ex2_hw(v) : exp2f(v);
+}
+
+// 1 - 2^v for v <= 0: with u = v ln 2, the Taylor series -(u + u^2/2 + u^3/6 + u^4/24)
+// where |u| < 1/16 (its next term is below 2^-24 relative there), else 1 - 2^v directly.
+template <bool FAST> __device__ __forceinline__ float one_minus_pow2(float v) {
+    const float u = v * 0.69314718055994531f;
     if (u > -0.0625f) return -u * fmaf(u, fmaf(u, fmaf(u, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-    return 1.0f - __expf(u);
+    return 1.0f - pow2<FAST>(v);
 }
 
 // One step for one channel; la2 = log2 sigmoid(lambda).  Returns h_t, and a_t in at.
+template <bool FAST>
 __device__ __forceinline__ float rglru_step(float h, float x, float ga, float gx, float la2,
                                             float c, float& at) {
-    const float r = sigmoidf_(ga);
+    const float r = sigm<FAST>(ga);
     const float l2 = (r > 0.0f) ? c * r * la2 : 0.0f;        // log2 a_t (a^0 = 1, also for a = 0)
-    at = exp2f(l2);
-    const float w = sqrtf(one_minus_exp(2.0f * 0.69314718055994531f * l2));
-    return fmaf(at, h, w * (sigmoidf_(gx) * x));
+    at = pow2<FAST>(l2);
+    const float om = one_minus_pow2<FAST>(2.0f * l2);          // 1 - a_t^2
+    const float w = FAST ? sqrt_hw(om) : sqrtf(om);
+    return fmaf(at, h, w * (sigm<FAST>(gx) * x));
 }
 
 constexpr int kWarps = 8;        // segments per tile
 constexpr int kLanes = 32;       // a lane owns channels 2*lane, 2*lane+1 of the CTA's 64
 
-template <typename TI, typename TO, int SEG>
+template <typename TI, typename TO, int SEG, bool FAST>
 __global__ void __launch_bounds__(kThreads, 2)
 rglru_scan_kernel(const TI* __restrict__ x, const TI* __restrict__ ga, const TI* __restrict__ gx,
                   const float* __restrict__ lam, const float* __restrict__ h0,
@@ -119,9 +147,9 @@ rglru_scan_kernel(const TI* __restrict__ x, const TI* __restrict__ ga, const TI*
                 const float2 av = Vec2<TI>::unpack(ba[u]);
                 const float2 gv = Vec2<TI>::unpack(bg[u]);
                 float at;
-                hl0 = rglru_step(hl0, xv.x, av.x, gv.x, la0, c, at);
+                hl0 = rglru_step<FAST>(hl0, xv.x, av.x, gv.x, la0, c, at);
                 pa0 *= at;
-                hl1 = rglru_step(hl1, xv.y, av.y, gv.y, la1, c, at);
+                hl1 = rglru_step<FAST>(hl1, xv.y, av.y, gv.y, la1, c, at);
                 pa1 *= at;
             }
             yl0[u] = hl0; yl1[u] = hl1; p0[u] = pa0; p1[u] = pa1;
@@ -158,9 +186,9 @@ cudaError_t launch_rg(const void* x, const void* ga, const void* gx, const float
     // D % 64 == 0 is checked by the caller; one CTA per (batch row, 64 channels)
     const long long blocks = (long long)b * (D / (2 * kLanes));
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // 16 steps per segment for 2-byte inputs, 8 for 4-byte ones (the same bytes)
-    constexpr int SEG = sizeof(TI) == 2 ? 16 : 8;
-    rglru_scan_kernel<TI, TO, SEG><<<(unsigned)blocks, kThreads, 0, s>>>(
+    // 12 steps per segment for 2-byte inputs, 8 for 4-byte ones (both within 128 registers)
+    constexpr int SEG = sizeof(TI) == 2 ? 12 : 8;
+    rglru_scan_kernel<TI, TO, SEG, sizeof(TI) == 2><<<(unsigned)blocks, kThreads, 0, s>>>(
         static_cast<const TI*>(x), static_cast<const TI*>(ga), static_cast<const TI*>(gx), lam,
         h0, static_cast<TO*>(y), h_last, b, T, D, c);
     cudaError_t err = cudaGetLastError();
