@@ -423,7 +423,8 @@ def bench_rglru(args, dist, rb, pk):
                         "initial state, fp32 y (rglru_scan)",
             "value": value, "unit": "steps/s (b*T per step)", "ms_per_step": ms_step,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": profile_traffic("rglru_scan_rglru.md", "rglru.cu"),
                          "algorithmic_bytes_per_launch": nbytes}}
 
 
