@@ -84,9 +84,10 @@ class Oracle:
         lib.oracle_msr_epilogue.argtypes = [P, P, P, I, I, I, I, ctypes.c_double, P, P]
         lib.oracle_chunkwise_backward.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, P]
         lib.oracle_rglru.argtypes = [P, P, P, P, P, P, P, I, I, I, ctypes.c_double]
+        lib.oracle_xpos_rotate.argtypes = [P, P, I, I, I, I, P, ctypes.c_longlong]
         for f in ("oracle_parallel", "oracle_recurrent", "oracle_recurrent_step",
                   "oracle_chunkwise", "oracle_brute", "oracle_msr_epilogue",
-                  "oracle_chunkwise_backward", "oracle_rglru"):
+                  "oracle_chunkwise_backward", "oracle_rglru", "oracle_xpos_rotate"):
             getattr(lib, f).restype = ctypes.c_int
         self.lib = lib
 
@@ -171,6 +172,15 @@ class Oracle:
                                      b, T, D, float(c)), "rglru")
         return (y, hl) if return_state else y
 
+    def xpos_rotate(self, x, theta, pos0: int = 0) -> np.ndarray:
+        """xPos rotation of [b,H,N,d] rows at positions pos0 + n; theta: [d/2]."""
+        x, th = _f64(x), _f64(theta)
+        b, H, N, d = x.shape
+        out = np.zeros_like(x)
+        _check(self.lib.oracle_xpos_rotate(_p(x), _p(out), b, H, N, d, _p(th), int(pos0)),
+               "xpos_rotate")
+        return out
+
     def msr_epilogue(self, y, g, eps: float, weight=None, bias=None) -> np.ndarray:
         """GroupNorm per (token, head) then swish(G) gate; y:[b,H,N,dv] g:[b,N,H*dv]."""
         y, g = _f64(y), _f64(g)
@@ -220,6 +230,10 @@ def chunkwise_backward(*a, **kw):
 
 def rglru(*a, **kw):
     return default().rglru(*a, **kw)
+
+
+def xpos_rotate(*a, **kw):
+    return default().xpos_rotate(*a, **kw)
 
 
 def map_units(fn, units, threads: int | None = None):

@@ -436,3 +436,32 @@ int oracle_rglru(const double* x, const double* gate_a, const double* gate_x,
         }
     return 0;
 }
+
+/*
+ * xPos rotation, [RN2] "Retention", eqs.(2)-(3) (their formulas were lost; the prose
+ * survives): Q_n becomes Q_n e^{i n theta} and K_m becomes K_m e^{i m theta}, so that
+ * the score of eq.(4), taken with the conjugate transpose, depends on n - m only (a
+ * relative position embedding).  Reading for real inputs: the pair of coordinates
+ * (2j, 2j+1) is one complex number z = x_{2j} + i x_{2j+1}, multiplied by
+ * e^{i p theta_j} at position p = pos0 + n:
+ *   out_{2j}   = x_{2j} cos(p theta_j) - x_{2j+1} sin(p theta_j)
+ *   out_{2j+1} = x_{2j} sin(p theta_j) + x_{2j+1} cos(p theta_j)
+ * x, out: [b][H][N][d] (d even), theta: [d/2].
+ */
+int oracle_xpos_rotate(const double* x, double* out, int b, int H, int N, int d,
+                       const double* theta, long long pos0) {
+    if (b < 0 || H < 0 || N < 0 || d <= 0 || d % 2 != 0) return -1;
+    for (long long row = 0; row < (long long)b * H * N; ++row) {
+        long long p = pos0 + row % N;
+        const double* xr = x + row * d;
+        double* orow = out + row * d;
+        for (int j = 0; j < d / 2; ++j) {
+            double ang = (double)p * theta[j];
+            double cs = cos(ang), sn = sin(ang);
+            double x0 = xr[2 * j], x1 = xr[2 * j + 1];
+            orow[2 * j] = x0 * cs - x1 * sn;
+            orow[2 * j + 1] = x0 * sn + x1 * cs;
+        }
+    }
+    return 0;
+}
