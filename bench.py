@@ -428,6 +428,32 @@ def bench_rglru(args, dist, rb, pk):
                          "algorithmic_bytes_per_launch": nbytes}}
 
 
+def bench_xpos(args, dist, rb, pk):
+    w = inputs.CHUNKWISE_LONG
+    q, k, _ = inputs.qkv(w, "cuda")
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    theta = [10000.0 ** (-j / (w.dk // 2)) for j in range(w.dk // 2)]
+
+    def step():
+        rb.retention_xpos_rotate(q, k, theta, 0, q_out=qo, k_out=ko)
+
+    steps = max(3, args.steps // 4)
+    ms, _ = timed(step, steps, 3, dist)
+    rb.check_device_error()
+    ms_step = ms / steps
+    value, _ = aggregate(dist, ms, w.b * w.N * steps)
+    nbytes = 4 * q.numel() * q.element_size()      # q and k, each read and written once
+    gbs = nbytes / (ms_step * 1e-3) / 1e9
+    del q, k, qo, ko
+    torch.cuda.empty_cache()
+    return {"workload": f"xpos: rotation of chunkwise_long's Q and K (b{w.b} H{w.H} N{w.N} "
+                        f"dk{w.dk}, bf16 in and out, theta_j = 10000^(-2j/dk), positions 0..N-1)",
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_launch": nbytes}}
+
+
 def cpu_baseline_leg():
     w = inputs.CHUNKWISE_LONG
     threads = max(1, min(os.cpu_count() or 1, w.H))
@@ -448,6 +474,7 @@ def run_ours(args, dist: Dist):
         extra["parallel"] = bench_parallel(args, dist, rb, pk)
         extra["backward"] = bench_backward(args, dist, rb, pk)
         extra["rglru"] = bench_rglru(args, dist, rb, pk)
+        extra["xpos"] = bench_xpos(args, dist, rb, pk)
     cpu = cpu_baseline_leg() if (dist.rank == 0 and dist.world == 1 and not args.no_cpu) else None
     if dist.rank != 0:
         return 0

@@ -233,6 +233,24 @@ int retention_parallel_gated(const void* q, const void* k, const void* v, const 
                              const float* weight, const float* bias, void* stream);
 
 /*
+ * xPos rotation of Q and K, [RN2] "Retention" eqs.(2)-(3) (formulas lost, prose kept):
+ * Q_n e^{i n theta} and K_m e^{i m theta}, "a relative position embedding", so that the
+ * retention score of eq.(4), taken with the conjugate transpose, depends on n - m only.
+ * For real inputs each pair of coordinates (2j, 2j+1) is one complex number:
+ *   out[.., n, 2j]   = x[.., n, 2j] cos(p theta_j) - x[.., n, 2j+1] sin(p theta_j)
+ *   out[.., n, 2j+1] = x[.., n, 2j] sin(p theta_j) + x[.., n, 2j+1] cos(p theta_j)
+ * at position p = pos0 + n.  Apply it to Q and K before retention_parallel,
+ * retention_chunkwise or retention_recurrent_step (pos0 = the first token's position).
+ * q, k: [b][H][N][dk] in in_dtype; q_out, k_out: the same shape in out_dtype.  k may
+ * be NULL (then k_out is ignored and only q is rotated).  q_out may equal q (and k_out
+ * k) when in_dtype == out_dtype; other overlaps are not allowed.  theta: HOST array of
+ * dk/2 finite doubles.  dk as for the retention calls.  One memory-bound launch.
+ */
+int retention_xpos_rotate(const void* q, const void* k, void* q_out, void* k_out,
+                          ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                          int dk, const double* theta, long long pos0, void* stream);
+
+/*
  * RG-LRU scan, the gated diagonal linear recurrence of the Griffin page ("Griffin ：
  * 將門控線性循環與局部注意力混合以實現高效的語言模型", section "實門線性循環單元
  * (RG-LRU)"), from the pre-activations of its two gates (the projections
@@ -294,7 +312,8 @@ enum {
     RET_KERNEL_PARALLEL_GATED_TC = 7, /* parallel form + gated GroupNorm, tensor cores */
     RET_KERNEL_CHUNKWISE_TC_PAIR = 8, /* chunkwise form, tensor cores on pairs of SMs */
     RET_KERNEL_CHUNKWISE_BACKWARD_SIMT = 9, /* chunkwise gradient, CUDA-core fp32 FMA   */
-    RET_KERNEL_RGLRU = 10           /* RG-LRU scan                                    */
+    RET_KERNEL_RGLRU = 10,          /* RG-LRU scan                                    */
+    RET_KERNEL_XPOS = 11            /* xPos rotation of Q and K                       */
 };
 
 /*

@@ -25,7 +25,7 @@ NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
                 5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair",
-                9: "chunkwise_backward_simt", 10: "rglru"}
+                9: "chunkwise_backward_simt", 10: "rglru", 11: "xpos"}
 
 _lib = None
 _lock = threading.Lock()
@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.retention_chunkwise.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp, vp, vp, vp]
             L.retention_chunkwise_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                                        i, i, i, dp, vp, vp, vp, vp]
+            L.retention_xpos_rotate.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, dp,
+                                                ctypes.c_longlong, vp]
             L.rglru_scan.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
             L.retention_recurrent_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, dp, vp]
             L.msr_epilogue.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, vp]
@@ -201,6 +203,29 @@ def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None
         _ptr(state_in), _ptr(dstate_out), _ptr(dstate_in), _stream(stream))
     _check("retention_chunkwise_backward", rc)
     return gq, gk, gv, dstate_in
+
+
+def retention_xpos_rotate(q, k, theta, pos0: int = 0, q_out=None, k_out=None, out_dtype=None,
+                          stream=None):
+    """xPos rotation of q (and k, if given) [b,H,N,dk] at positions pos0 + n; theta: dk/2
+    angles.  Returns (q_out, k_out); pass q_out=q (k_out=k) to rotate in place."""
+    b, H, N, dk = q.shape
+    if k is not None and (k.shape != q.shape or k.dtype != q.dtype):
+        raise TypeError("q and k must share shape and dtype")
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if q_out is None:
+        q_out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if k is not None and k_out is None:
+        k_out = torch.empty(k.shape, dtype=q_out.dtype, device=k.device)
+    th = [float(t) for t in theta]
+    if len(th) != dk // 2:
+        raise ValueError(f"theta has {len(th)} entries, expected dk/2={dk // 2}")
+    tarr = (ctypes.c_double * max(len(th), 1))(*th)
+    rc = lib().retention_xpos_rotate(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out),
+                                     _dtype_code(q.dtype), _dtype_code(q_out.dtype), b, H, N,
+                                     dk, tarr, int(pos0), _stream(stream))
+    _check("retention_xpos_rotate", rc)
+    return q_out, k_out
 
 
 def rglru_scan(x, gate_a, gate_x, lambda_, h0=None, c: float = 8.0, out=None,

@@ -90,6 +90,9 @@ cudaError_t launch_chunkwise_backward_simt(const void* q, const void* k, const v
 cudaError_t launch_rglru_scan(const void* x, const void* ga, const void* gx, const float* lam,
                               const float* h0, void* y, float* h_last, int in_bf16, int out_bf16,
                               int b, int T, int D, float c, cudaStream_t s);
+cudaError_t launch_xpos_rotate(const void* q, const void* k, void* q_out, void* k_out,
+                               int in_bf16, int out_bf16, int b, int H, int N, int d,
+                               const double* theta, long long pos0, cudaStream_t s);
 // Tensor-core paths: return cudaErrorNotSupported when the shape is outside
 // what the kernel handles, so the caller can pick the CUDA-core kernel.
 cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, void* o,

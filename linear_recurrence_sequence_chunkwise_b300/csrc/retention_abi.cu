@@ -251,6 +251,25 @@ int msr_epilogue(const void* y, const void* g, void* out, ret_dtype y_dtype, ret
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+int retention_xpos_rotate(const void* q, const void* k, void* q_out, void* k_out,
+                          ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
+                          int dk, const double* theta, long long pos0, void* stream) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (!dims_ok(dk, 16)) return RET_ERR_UNSUPPORTED;
+    if (b == 0 || H == 0 || N == 0) return RET_OK;
+    if (!q || !q_out || !theta || (k && !k_out)) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(q_out) || (k && (!aligned16(k) || !aligned16(k_out))))
+        return RET_ERR_ALIGN;
+    if (in_dtype != out_dtype && (q_out == q || (k && k_out == k))) return RET_ERR_DTYPE;
+    for (int j = 0; j < dk / 2; ++j)
+        if (!isfinite(theta[j])) return RET_ERR_UNSUPPORTED;
+    return cuda_status(ret::launch_xpos_rotate(q, k, q_out, k ? k_out : nullptr,
+                                               in_dtype == RET_BF16, out_dtype == RET_BF16, b,
+                                               H, N, dk, theta, pos0,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 int rglru_scan(const void* x, const void* gate_a, const void* gate_x, const float* lambda_,
                const float* h0, void* y, float* h_last, ret_dtype in_dtype,
                ret_dtype out_dtype, int b, int T, int D, float c, void* stream) {

@@ -38,7 +38,8 @@ def test_exports_every_declared_function(L):
                           "retention_chunkwise_host", "retention_chunkwise_host_workspace_bytes",
                           "retention_chunkwise_host_noalloc",
                           "retention_chunkwise_host_static_scratch_bytes",
-                          "retention_chunkwise_backward", "rglru_scan"}
+                          "retention_chunkwise_backward", "rglru_scan",
+                          "retention_xpos_rotate"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
@@ -180,6 +181,30 @@ def test_rglru_rejections(L):
     assert rg(L, hl=MIS) == binding.RET_ERR_ALIGN
     assert rg(L, b=0, x=NUL, ga=NUL, gx=NUL, lam=NUL, y=NUL) == binding.RET_OK
     assert rg(L, T=0, x=NUL, ga=NUL, gx=NUL, lam=NUL, y=NUL) == binding.RET_OK
+    assert binding.kernel_launches() == before
+
+
+def xp(L, q=A, k=A, qo=A2, ko=A2, it=1, ot=1, b=1, H=2, N=64, dk=64, th=None, pos0=0):
+    th = (ctypes.c_double * 32)(*([0.1] * 32)) if th is None else th
+    return L.retention_xpos_rotate(q, k, qo, ko, it, ot, b, H, N, dk, th,
+                                   ctypes.c_longlong(pos0), S)
+
+
+def test_xpos_rejections(L):
+    before = binding.kernel_launches()
+    assert xp(L, N=-1) == binding.RET_ERR_SHAPE
+    assert xp(L, it=3) == binding.RET_ERR_DTYPE
+    assert xp(L, dk=24) == binding.RET_ERR_UNSUPPORTED
+    assert xp(L, dk=512) == binding.RET_ERR_UNSUPPORTED
+    assert xp(L, q=NUL) == binding.RET_ERR_NULL
+    assert xp(L, ko=NUL) == binding.RET_ERR_NULL
+    assert xp(L, th=ctypes.POINTER(ctypes.c_double)()) == binding.RET_ERR_NULL
+    assert xp(L, qo=MIS) == binding.RET_ERR_ALIGN
+    assert xp(L, k=MIS) == binding.RET_ERR_ALIGN
+    assert xp(L, qo=A, ot=0) == binding.RET_ERR_DTYPE        # in place across dtypes
+    bad = (ctypes.c_double * 32)(*([0.1] * 31 + [float("inf")]))
+    assert xp(L, th=bad) == binding.RET_ERR_UNSUPPORTED
+    assert xp(L, b=0, q=NUL, k=NUL, qo=NUL, ko=NUL) == binding.RET_OK
     assert binding.kernel_launches() == before
 
 
