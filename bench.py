@@ -462,6 +462,11 @@ def cpu_baseline_leg():
             "sample": desc + f" ({dt:.1f} s wall)"}
 
 
+# the legs reported beside the headline, in this order
+EXTRA_LEGS = {"decode": bench_decode, "parallel": bench_parallel, "backward": bench_backward,
+              "rglru": bench_rglru, "xpos": bench_xpos}
+
+
 def run_ours(args, dist: Dist):
     from linear_recurrence_sequence_chunkwise_b300 import binding as rb
     rb.lib()
@@ -470,11 +475,9 @@ def run_ours(args, dist: Dist):
     main = bench_chunkwise(args, dist, rb, pk, out_dtype)
     extra = {}
     if not args.only_headline:
-        extra["decode"] = bench_decode(args, dist, rb, pk)
-        extra["parallel"] = bench_parallel(args, dist, rb, pk)
-        extra["backward"] = bench_backward(args, dist, rb, pk)
-        extra["rglru"] = bench_rglru(args, dist, rb, pk)
-        extra["xpos"] = bench_xpos(args, dist, rb, pk)
+        for name in args.legs.split(","):
+            if name:
+                extra[name] = EXTRA_LEGS[name](args, dist, rb, pk)
     cpu = cpu_baseline_leg() if (dist.rank == 0 and dist.world == 1 and not args.no_cpu) else None
     if dist.rank != 0:
         return 0
@@ -500,6 +503,7 @@ PROFILE_CASES = {
     "parallel": "parallel_norm (b8 H8 N2048 dk256 dv512, all normalisations) + epilogue",
     "backward": "backward (b4 H16 N2048 dk256 dv512 chunk 64), bf16 in, fp32 gradients (1.1 GB)",
     "rglru": "rglru (b8 T4096 D4096), bf16 x and gates, fp32 y (1.3 GB)",
+    "xpos": "xpos rotation of chunkwise_long's Q and K (b1 H16 N32768 dk256, bf16, 1.1 GB)",
 }
 
 
@@ -528,6 +532,12 @@ def run_profile(case: str) -> int:
                       for d in (w.dk, w.dk, w.dv))
         calls = [lambda: rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk,
                                                          grads=grads)]
+    elif case == "xpos":
+        w = inputs.CHUNKWISE_LONG
+        q, k, _ = inputs.qkv(w, "cuda")
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        theta = [10000.0 ** (-j / (w.dk // 2)) for j in range(w.dk // 2)]
+        calls = [lambda: rb.retention_xpos_rotate(q, k, theta, 0, q_out=qo, k_out=ko)]
     elif case == "rglru":
         w = inputs.RGLRU
         x, ga, gx, lam = inputs.rglru_inputs(w, "cuda")
@@ -556,10 +566,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--only-headline", action="store_true")
+    ap.add_argument("--legs", default=",".join(EXTRA_LEGS),
+                    help="comma-separated legs reported beside the headline "
+                         f"(default all: {','.join(EXTRA_LEGS)})")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES), default=None,
                     help="run two untimed calls of one reduced workload (for ncu) and exit")
     args = ap.parse_args(argv)
+    unknown = [x for x in args.legs.split(",") if x and x not in EXTRA_LEGS]
+    if unknown:
+        ap.error(f"unknown legs {unknown}; choose from {sorted(EXTRA_LEGS)}")
     if args.profile:
         return run_profile(args.profile)
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
