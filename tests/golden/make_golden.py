@@ -25,6 +25,21 @@ def cases():
     yield "parallel_f7", oracle.parallel(q, k, v, w.gamma, 7)
     yield "chunkwise_B16", oracle.chunkwise(q, k, v, w.gamma, 16)
     yield "epilogue_f7", oracle.msr_epilogue(oracle.parallel(q, k, v, w.gamma, 7), g, 1e-5)
+    # gradient of the chunkwise form with both states, upstream gradient N(0,1)
+    do = inputs.randn((w.b, w.H, w.N, w.dv), w.seed + 10, 1.0, "f32")
+    s0 = inputs.randn((w.b, w.H, w.dk, w.dv), w.seed + 11, 0.1, "f32")
+    ds = inputs.randn((w.b, w.H, w.dk, w.dv), w.seed + 12, 0.1, "f32")
+    gq, gk, gv, gs = oracle.chunkwise_backward(q, k, v, do, w.gamma, state_in=s0, dstate_out=ds)
+    yield "backward_dq", gq
+    yield "backward_dk", gk
+    yield "backward_dv", gv
+    yield "backward_ds0", gs
+    # xPos rotation of q at positions 100.., theta_j = 10000^(-2j/dk)
+    yield "xpos_q", oracle.xpos_rotate(q, [10000.0 ** (-j / 8) for j in range(8)], 100)
+    # RG-LRU scan on [1, 64, 16] (x, gate pre-activations N(0,1), Lambda of the page's init)
+    x, ga, gx = (inputs.randn((1, 64, 16), w.seed + 20 + i, 1.0, "f32") for i in range(3))
+    yield "rglru", oracle.rglru(x, ga, gx, inputs.rglru_lambda(16, w.seed + 23),
+                                inputs.randn((1, 16), w.seed + 24, 1.0, "f32"))
 
 
 def sample_idx(n, count=48, seed=7):
