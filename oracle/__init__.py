@@ -192,6 +192,34 @@ class Oracle:
         return out
 
 
+def msr_layer(x, wq, wk, wv, wg, wo, gamma, theta=None, flags: int = 0, eps: float = 1e-5,
+              pos0: int = 0, chunk: int | None = None):
+    """Gated multi-scale retention layer, [RN2] "門控多尺度 Retention" (its formula was
+    lost; the prose and the calls it names survive), composed from numpy matmuls and
+    the oracle functions above:
+        Q = xPos(X W_Q), K = xPos(X W_K), V = X W_V     per head (head h: columns
+                                                       h*dk.. of W_Q, W_K; h*dv.. of W_V)
+        Y = retention(Q, K, V, gamma_h)                parallel form with `flags`, or the
+                                                       chunkwise form when `chunk` is set
+        out = (swish(X W_G) (.) GroupNorm_h(Y)) W_O
+    x: [b, N, D]; wq, wk: [D, H*dk]; wv, wg: [D, H*dv]; wo: [H*dv, D']; gamma: [H];
+    theta: [dk/2] xPos angles (None: no rotation).  Returns [b, N, D']."""
+    x = _f64(x)
+    wq, wk, wv, wg, wo = (_f64(w) for w in (wq, wk, wv, wg, wo))
+    b, N, _ = x.shape
+    H = len(gamma)
+    dk, dv = wq.shape[1] // H, wv.shape[1] // H
+
+    def heads(t, d):
+        return np.ascontiguousarray(t.reshape(b, N, H, d).transpose(0, 2, 1, 3))
+
+    q, k, v = heads(x @ wq, dk), heads(x @ wk, dk), heads(x @ wv, dv)
+    if theta is not None:
+        q, k = xpos_rotate(q, theta, pos0), xpos_rotate(k, theta, pos0)
+    y = chunkwise(q, k, v, gamma, chunk) if chunk else parallel(q, k, v, gamma, flags)
+    return msr_epilogue(y, x @ wg, eps) @ wo
+
+
 def default() -> Oracle:
     global _default
     with _lock:
