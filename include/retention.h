@@ -19,9 +19,11 @@
  * transpose of eq.(4) is a transpose.
  *
  * Common rules for every call
- *   - Pointers named q, k, v, o, y, g, out, state, state_in, state_out are
- *     DEVICE pointers to contiguous row-major arrays, 16-byte aligned.  The
- *     caller owns every buffer; the library allocates nothing.
+ *   - Every tensor pointer (q, k, v, o, y, g, out, state, state_in, state_out,
+ *     dout, grad_*, dstate_*, q_out, k_out, x, gate_*, lambda_, h0, h_last) is a
+ *     DEVICE pointer to a contiguous row-major array, 16-byte aligned, unless its
+ *     declaration says HOST.  The caller owns every buffer; the library allocates
+ *     nothing (retention_chunkwise_host_noalloc's file-scope scratch aside).
  *   - gamma is a HOST pointer to H doubles, each in [0, 1].
  *   - Calls are asynchronous on the CUDA stream `stream` (a cudaStream_t; NULL
  *     means the legacy default stream).  Argument checks run on the host
