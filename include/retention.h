@@ -152,7 +152,8 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
  * Argument checks (those of retention_chunkwise, plus seg_len > 0 with seg_len % chunk
  * == 0 and N % seg_len == 0, and the workspace size: RET_ERR_SHAPE) run before the
  * first copy.  A CUDA error or a failed segment returns its status; earlier segments
- * may then have been written.
+ * may then have been written, and stream still waits for the copies already queued on
+ * the copy streams (so the workspace is free once stream reaches that point).
  */
 int retention_chunkwise_host(const void* q, const void* k, const void* v, void* o,
                              ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int N,
@@ -173,7 +174,9 @@ size_t retention_chunkwise_host_workspace_bytes(ret_dtype in_dtype, ret_dtype ou
  * retention_chunkwise_host without a caller workspace: the carried state and the segment
  * buffers live in a file-scope device array of retention_chunkwise_host_static_scratch_bytes()
  * bytes, reserved on each device when the library's module loads there; its address is
- * looked up once per device.  Arguments and behaviour otherwise as retention_chunkwise_host.
+ * looked up on the first call on a device (and again if that device's context changed,
+ * e.g. after cudaDeviceReset), so make that first call before any stream capture.
+ * Arguments and behaviour otherwise as retention_chunkwise_host.
  * A call whose workspace (retention_chunkwise_host_workspace_bytes) exceeds the scratch
  * returns RET_ERR_SHAPE, like every other argument check, before any device access.  The
  * scratch is shared by all calls on a device: they must not overlap in time (issue them

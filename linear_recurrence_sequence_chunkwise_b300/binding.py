@@ -274,7 +274,8 @@ def retention_chunkwise_host(q, k, v, gamma, chunk: int, out, seg_len: int, stat
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k and v must share one dtype")
     dev = torch.device("cuda", torch.cuda.current_device())
-    if workspace is None:
+    owned = workspace is None
+    if owned:
         nbytes = chunkwise_host_workspace_bytes(q.dtype, out.dtype, b, H, dk, dv, seg_len)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     if copy_streams is None:
@@ -287,6 +288,12 @@ def retention_chunkwise_host(q, k, v, gamma, chunk: int, out, seg_len: int, stat
         _ptr(state_out), seg_len, ctypes.c_void_p(workspace.data_ptr()),
         ctypes.c_size_t(workspace.numel()), _stream(stream),
         ctypes.c_void_p(copy_streams[0].cuda_stream), ctypes.c_void_p(copy_streams[1].cuda_stream))
+    if owned:
+        # The workspace was allocated on the current stream, but the queued copies and
+        # kernels use it on `stream` and the copy streams: keep the caching allocator from
+        # handing the block out again before that work is done.
+        for s in (stream or torch.cuda.current_stream(dev), *copy_streams):
+            workspace.record_stream(s)
     _check("retention_chunkwise_host", rc)
     return out
 

@@ -11,6 +11,8 @@
 
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace {
@@ -77,21 +79,48 @@ __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_static_scratch on the current device, looked up once per device.
+// The current CUDA context (driver entry point fetched through the runtime, so the
+// library needs no link to libcuda); nullptr if it cannot be queried.
+void* current_context() {
+    using Fn = CUresult (*)(CUcontext*);
+    static Fn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<Fn>(p);
+        return static_cast<Fn>(nullptr);
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of g_static_scratch on the current device, looked up once per device
+// and context: after cudaDeviceReset the module loads again in a new context, possibly at
+// another address, so a changed context triggers a new lookup.
 cudaError_t static_scratch(void** out) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static void* ctx[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // cudaFree(0) makes the device's primary context current if no context is yet
+    e = cudaFree(nullptr);
+    if (e != cudaSuccess) return e;
+    void* const cur = current_context();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || !cur || cur != ctx[dev]) {
         e = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
         if (e != cudaSuccess) {
             addr[dev] = nullptr;
+            ctx[dev] = nullptr;
             return e;
         }
+        ctx[dev] = cur;
     }
     *out = addr[dev];
     return cudaSuccess;
@@ -149,12 +178,13 @@ int retention_chunkwise_host(const void* q, const void* k, const void* v, void* 
     const int nseg = N / seg_len;
 
     // events live for this call only; destroying a recorded event frees it once it completes
-    cudaEvent_t ev_start, h2d_done[2], comp_done[2], d2h_done[2];
+    cudaEvent_t ev_start, h2d_done[2], comp_done[2], d2h_done[2], join_h, join_d;
     cudaEvent_t* all[] = {&ev_start, &h2d_done[0], &h2d_done[1], &comp_done[0], &comp_done[1],
-                          &d2h_done[0], &d2h_done[1]};
+                          &d2h_done[0], &d2h_done[1], &join_h, &join_d};
+    constexpr int kEvents = sizeof(all) / sizeof(all[0]);
     int made = 0;
     cudaError_t e = cudaSuccess;
-    for (; made < 7 && e == cudaSuccess; ++made)
+    for (; made < kEvents && e == cudaSuccess; ++made)
         e = cudaEventCreateWithFlags(all[made], cudaEventDisableTiming);
     auto finish = [&](int rc) {
         for (int i = 0; i < made; ++i) cudaEventDestroy(*all[i]);
@@ -164,11 +194,19 @@ int retention_chunkwise_host(const void* q, const void* k, const void* v, void* 
         --made;   // the failed one was not created
         return finish(status_of(e));
     }
+    // An error after copies were queued: stream still waits for whatever the copy streams
+    // hold, so that work already queued never outlives the ordering the header promises
+    // (best effort: the calls below may fail too if the error came from the device).
+    auto fail = [&](int rc) {
+        if (cudaEventRecord(join_h, hs) == cudaSuccess) cudaStreamWaitEvent(cs, join_h, 0);
+        if (cudaEventRecord(join_d, ds) == cudaSuccess) cudaStreamWaitEvent(cs, join_d, 0);
+        return finish(rc);
+    };
     // the copy streams start after the work already queued on the compute stream
     e = cudaEventRecord(ev_start, cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hs, ev_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ds, ev_start, 0);
-    if (e != cudaSuccess) return finish(status_of(e));
+    if (e != cudaSuccess) return fail(status_of(e));
 
     for (int s = 0; s < nseg; ++s) {
         const int j = s & 1;
@@ -189,11 +227,11 @@ int retention_chunkwise_host(const void* q, const void* k, const void* v, void* 
         // compute, continuing from the state the previous segment left
         if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, h2d_done[j], 0);
         if (e == cudaSuccess && s >= 2) e = cudaStreamWaitEvent(cs, d2h_done[j], 0);
-        if (e != cudaSuccess) return finish(status_of(e));
+        if (e != cudaSuccess) return fail(status_of(e));
         const int rc = retention_chunkwise(qd[j], kd[j], vd[j], od[j], in_dtype, out_dtype, b, H,
                                            seg_len, dk, dv, chunk, gamma,
                                            s == 0 ? state_in : st, st, stream);
-        if (rc != RET_OK) return finish(rc);
+        if (rc != RET_OK) return fail(rc);
         e = cudaEventRecord(comp_done[j], cs);
         // device -> host
         if (e == cudaSuccess) e = cudaStreamWaitEvent(ds, comp_done[j], 0);
@@ -203,12 +241,13 @@ int retention_chunkwise_host(const void* q, const void* k, const void* v, void* 
                                   od[j], w, w, rows, cudaMemcpyDeviceToHost, ds);
         }
         if (e == cudaSuccess) e = cudaEventRecord(d2h_done[j], ds);
-        if (e != cudaSuccess) return finish(status_of(e));
+        if (e != cudaSuccess) return fail(status_of(e));
     }
     // the compute stream orders everything: the last copies out, then the final state
     e = cudaStreamWaitEvent(cs, d2h_done[(nseg - 1) & 1], 0);
     if (e == cudaSuccess && nseg >= 2) e = cudaStreamWaitEvent(cs, d2h_done[nseg & 1], 0);
-    if (e == cudaSuccess && state_out)
+    if (e != cudaSuccess) return fail(status_of(e));
+    if (state_out)
         e = cudaMemcpyAsync(state_out, st, (size_t)b * H * dk * dv * sizeof(float),
                             cudaMemcpyDeviceToDevice, cs);
     return finish(status_of(e));

@@ -24,14 +24,22 @@
 // pairs instead of dv/64 CTAs.  The pair costs one duplicated quarter of the score tile
 // (the even CTA's rows against keys 128-255, all masked) and of P.V.
 //
-// Roles (320 threads per CTA): warp 0 issues this CTA's TMA loads (Q, K and the K^T
-// operand complete on the even CTA's barriers, V on a local one), warp 1 allocates
-// tensor memory (both CTAs, collectively) and, in the even CTA, issues the MMAs, warps
-// 2-5 turn this CTA's score rows into P and then write its output rows (coalesced stores
-// from registers), warps 6-9 copy the peer half of this CTA's state rows (into the
-// peer's shared memory) and scale V.  Warp w reaches TMEM lanes 32*(w%4)..+31.  Every wait is bounded;
-// a wait that gives up sets the device error word and both CTAs' abort flags, and the
-// CTAs unwind, meet at a final cluster barrier and free their tensor memory.
+// Roles (576 threads = 18 warps per CTA).  The transform work of a chunk is spread over
+// sixteen warps in two groups that run side by side, so that no group has more than one
+// task on the path between two MMAs:
+//   warp 0      TMA loads of this CTA (Q, K and the K^T operand complete on the even CTA's
+//               barriers, V on a local one) and L2 prefetches one chunk ahead
+//   warp 1      tensor-memory allocation (both CTAs, collectively); in the even CTA the
+//               MMA issuer
+//   warps 2-9   scores -> P (two warps per TMEM lane quarter, one per 128-key half), then
+//               the chunk's output rows (one per 64-column half), coalesced stores
+//   warps 10-17 state copy (two warps per lane quarter: this CTA's own 64 value columns
+//               into its own shared memory, the peer's 64 into the peer's, 64-byte row
+//               pieces), the rescale
+//               R <- g^B R, then V -> Vz (one key row per thread)
+// Warp w reaches TMEM lanes 32*(w%4)..+31.  Every wait is bounded; a wait that gives up
+// sets the device error word and both CTAs' abort flags, and the CTAs unwind, meet at a
+// final cluster barrier and free their tensor memory.
 //
 // Tensor memory per CTA (512 columns x 128 lanes, fp32):
 //   [  0,256) S: this CTA's 128 query rows x 256 keys; P written in place as bf16 pairs
@@ -41,12 +49,15 @@
 // Shared memory per CTA (1024-aligned, 224 KB), each box 128 rows x 64 bf16, 128B swizzle:
 //   Q   64 KB  own 128 query rows x 4 dk boxes
 //   K   64 KB  own 128 keys x 4 dk boxes (S); after S the K^T operand of the state update:
-//              all 256 keys x own 128 dk columns (2 key blocks x 2 dk boxes; the own key
-//              block's boxes stay from S, the peer key block is loaded)
+//              key block j (keys 128j..) x own 128 dk columns in boxes 2j, 2j+1.  The own
+//              key block's boxes stay from S; the peer key block is loaded into the two
+//              boxes S no longer needs (the same offsets in both CTAs)
 //   V   32 KB  256 keys x own 64 value columns (scaled in place to Vz)
 //   Rhi 32 KB, Rlo 32 KB  bf16 copy of R_{i-1}: 256 dk rows x own 64 columns
-// MMA order in a chunk: S, Q.R, K^T.Vz, P.Vz; the K area is reloaded with the K^T operand
-// during Q.R and with the next chunk's keys during P.Vz.
+// MMA order in a chunk: S (dk boxes 0-1, then 2-3), Q.R, K^T.Vz (key block 0, then 1),
+// P.Vz.  Commits between the halves free shared memory early: after S's first half the
+// odd CTA loads its peer key block (boxes 0-1), after its second half the even CTA
+// (boxes 2-3); after K^T.Vz's first half the next chunk's keys load into boxes 0-1.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
@@ -58,7 +69,7 @@ __device__ unsigned g_err_chunkwise_pair;
 
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 576;
 constexpr int kB = 256;                        // chunk length
 constexpr int kDk = 256;
 constexpr int kBox = 128 * 128;                // 128 rows x 64 bf16
@@ -69,8 +80,9 @@ constexpr int kRhiOff = kVOff + 2 * kBox;
 constexpr int kRloOff = kRhiOff + 2 * kBox;
 constexpr int kSmemBytes = kRloOff + 2 * kBox;  // 229376
 constexpr uint32_t kTS = 0, kTO = 256, kTR = 384;
-constexpr uint32_t kPairArrivals = 8;          // 4 warps in each CTA
+constexpr uint32_t kPairArrivals = 16;         // 8 warps in each CTA
 constexpr uint16_t kBoth = 3;                  // multicast mask: both CTAs of the pair
+constexpr int kFirstP = 2, kFirstR = 10;       // first warp of each transform group
 
 struct Decay {
     float l2g[kMaxHeads];   // log2(gamma)
@@ -80,12 +92,15 @@ struct Decay {
 
 struct Bars {
     // the even CTA's copies count both CTAs' work
-    uint64_t q_full, k_full, kt_full;              // pair loads (transaction bytes)
+    uint64_t q_full, k_full0, k_full1;             // pair loads: Q; K dk boxes 0-1 / 2-3
+    uint64_t kt_full0, kt_full1;                   // peer key block of K^T in boxes 0-1 / 2-3
     uint64_t vz_ready, p_ready, rcopy, o_free;     // warp arrivals of both CTAs
 
     // each CTA's own copy, arrived on by the MMA commits (multicast)
-    uint64_t q_empty, k_empty, kt_empty, v_empty;
-    uint64_t s_full, o_full, r_done;
+    uint64_t q_empty;                              // Q.R done: Q area free
+    uint64_t s_half, s_full;                       // S done with dk boxes 0-1 / all of S
+    uint64_t kt_empty0, kt_empty1;                 // K^T.Vz done with boxes 0-1 / 2-3
+    uint64_t v_empty, o_full, r_done;              // P.Vz done (V free, O complete); K^T.Vz done
     uint64_t v_full;                               // local V load
     uint64_t drain;
 };
@@ -131,12 +146,13 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full, 1); mbar_init(&bars.kt_full, 1);
+        mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full0, 1); mbar_init(&bars.k_full1, 1);
+        mbar_init(&bars.kt_full0, 1); mbar_init(&bars.kt_full1, 1);
         mbar_init(&bars.vz_ready, kPairArrivals); mbar_init(&bars.p_ready, kPairArrivals);
-        mbar_init(&bars.rcopy, 2 * kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
-        mbar_init(&bars.q_empty, 1); mbar_init(&bars.k_empty, 1);
-        mbar_init(&bars.kt_empty, 1); mbar_init(&bars.v_empty, 1);
-        mbar_init(&bars.s_full, 1); mbar_init(&bars.o_full, 1); mbar_init(&bars.r_done, 1);
+        mbar_init(&bars.rcopy, kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
+        mbar_init(&bars.q_empty, 1); mbar_init(&bars.s_half, 1); mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.kt_empty0, 1); mbar_init(&bars.kt_empty1, 1);
+        mbar_init(&bars.v_empty, 1); mbar_init(&bars.o_full, 1); mbar_init(&bars.r_done, 1);
         mbar_init(&bars.v_full, 1); mbar_init(&bars.drain, 1);
         fence_barrier_init();
     }
@@ -157,7 +173,9 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv);
-            const uint32_t qf = lead(&bars.q_full), kf = lead(&bars.k_full), ktf = lead(&bars.kt_full);
+            const uint32_t qf = lead(&bars.q_full), kf0 = lead(&bars.k_full0),
+                           kf1 = lead(&bars.k_full1);
+            const uint32_t ktf = lead(rank == 0 ? &bars.kt_full1 : &bars.kt_full0);
             const int rowbase = bh * N;
             const int own = 128 * (int)rank, other = 128 * (int)peer;
             const int vcol = blk * 128 + 64 * (int)rank;
@@ -180,26 +198,37 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             };
             prefetch(0);
             for (int c = 0; c < nchunks && ok; ++c) {
+                const uint32_t pp = (uint32_t)(c - 1) & 1u;
                 const int r0 = rowbase + c * kB;
                 // Q: own query rows, all dk (after the previous chunk's Q.R)
-                if (c > 0 && !w(&bars.q_empty, (c - 1) & 1)) break;
+                if (c > 0 && !w(&bars.q_empty, pp)) break;
                 if (rank == 0) { mbar_arrive_expect_tx(&bars.q_full, 2 * 4 * kBox); ++armed_q; }
                 for (int a = 0; a < 4; ++a) tma_load_2d_pair(sq + a * kBox, &mq, 64 * a, r0 + own, qf);
-                // K: own keys, all dk (after the previous chunk's K^T.Vz)
-                if (c > 0 && !w(&bars.kt_empty, (c - 1) & 1)) break;
-                if (rank == 0) { mbar_arrive_expect_tx(&bars.k_full, 2 * 4 * kBox); ++armed_k; }
-                for (int a = 0; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf);
+                // K: own keys; dk boxes 0-1 once K^T.Vz has read key block 0, boxes 2-3 once
+                // it has read key block 1
+                if (c > 0 && !w(&bars.kt_empty0, pp)) break;
+                if (rank == 0) {
+                    mbar_arrive_expect_tx(&bars.k_full0, 2 * 2 * kBox);
+                    mbar_arrive_expect_tx(&bars.k_full1, 2 * 2 * kBox);
+                    ++armed_k;
+                }
+                for (int a = 0; a < 2; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf0);
+                if (c > 0 && !w(&bars.kt_empty1, pp)) break;
+                for (int a = 2; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf1);
                 // V: all keys of the chunk, own 64 value columns (after the previous P.Vz)
-                if (c > 0 && !w(&bars.v_empty, (c - 1) & 1)) break;
+                if (c > 0 && !w(&bars.v_empty, pp)) break;
                 mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
                 for (int j = 0; j < 2; ++j) tma_load_2d(sv + j * kBox, &mv, vcol, r0 + 128 * j, &bars.v_full);
                 ++v_loads;
-                // K^T operand of the state update: all keys x own dk half, as key block j,
-                // dk box m at (2j + m) boxes.  The own key block's boxes of the own dk half
-                // already sit there (K boxes 2*rank+m); once S has read the other two boxes,
-                // the peer key block takes their place (the same offsets in both CTAs).
-                if (!w(&bars.k_empty, c & 1)) break;
-                if (rank == 0) { mbar_arrive_expect_tx(&bars.kt_full, 2 * 2 * kBox); ++armed_kt; }
+                // K^T operand of the state update: the peer key block x own dk half goes
+                // into boxes 2*peer, 2*peer+1 once S has read them (the odd CTA's after S's
+                // first half, the even CTA's after all of S)
+                if (!w(rank == 1 ? &bars.s_half : &bars.s_full, (uint32_t)c & 1u)) break;
+                if (rank == 0) {
+                    mbar_arrive_expect_tx(&bars.kt_full0, 2 * kBox);
+                    mbar_arrive_expect_tx(&bars.kt_full1, 2 * kBox);
+                    ++armed_kt;
+                }
                 for (int m = 0; m < 2; ++m)
                     tma_load_2d_pair(sk + (2 * (int)peer + m) * kBox, &mk, 64 * (2 * (int)rank + m),
                                      r0 + other, ktf);
@@ -211,8 +240,14 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (v_loads) mbar_wait(&bars.v_full, (v_loads - 1) & 1, nullptr, 100000000ull);
                 if (rank == 0) {
                     if (armed_q) mbar_wait(&bars.q_full, (armed_q - 1) & 1, nullptr, 100000000ull);
-                    if (armed_k) mbar_wait(&bars.k_full, (armed_k - 1) & 1, nullptr, 100000000ull);
-                    if (armed_kt) mbar_wait(&bars.kt_full, (armed_kt - 1) & 1, nullptr, 100000000ull);
+                    if (armed_k) {
+                        mbar_wait(&bars.k_full0, (armed_k - 1) & 1, nullptr, 100000000ull);
+                        mbar_wait(&bars.k_full1, (armed_k - 1) & 1, nullptr, 100000000ull);
+                    }
+                    if (armed_kt) {
+                        mbar_wait(&bars.kt_full0, (armed_kt - 1) & 1, nullptr, 100000000ull);
+                        mbar_wait(&bars.kt_full1, (armed_kt - 1) & 1, nullptr, 100000000ull);
+                    }
                 }
             }
         }
@@ -235,21 +270,35 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (ok && !mbar_wait_cl(bar, par, abort_p)) { ok = false; fail(); }
                 return ok;
             };
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const uint32_t ph = (uint32_t)c & 1u;
-                // S = Q K^T (the previous P.Vz, issued earlier, reads the S columns first:
-                // tcgen05.mma operations of one thread run in issue order)
-                if (!w(&bars.q_full, ph) || !w(&bars.k_full, ph)) break;
-                tc_fence_after();
+            auto s_boxes = [&](int a0) {
 #pragma unroll 1
-                for (int a = 0; a < 4; ++a)
+                for (int a = a0; a < a0 + 2; ++a)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t off = (uint64_t)((a * kBox + kk * 32) >> 4);
                         mma_pair(tmem + kTS, dQ + off, dK + off, id_s, (a | kk) != 0);
                     }
+            };
+            auto kv_block = [&](int j) {
+#pragma unroll
+                for (int t = 8 * j; t < 8 * j + 8; ++t) {
+                    const uint64_t ka = (uint64_t)(((t >> 3) * 2 * kBox + (t & 7) * 2048) >> 4);
+                    const uint64_t off = (uint64_t)((t * 2048) >> 4);
+                    mma_pair(tmem + kTR, dKT + ka, dV + off, id_r, 1);
+                }
+            };
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const uint32_t ph = (uint32_t)c & 1u;
+                // S = Q K^T (the previous P.Vz, issued earlier, reads the S columns first:
+                // tcgen05.mma operations of one thread run in issue order)
+                if (!w(&bars.q_full, ph) || !w(&bars.k_full0, ph)) break;
+                tc_fence_after();
+                s_boxes(0);
+                mma_commit_pair(&bars.s_half, kBoth);
+                if (!w(&bars.k_full1, ph)) break;
+                tc_fence_after();
+                s_boxes(2);
                 mma_commit_pair(&bars.s_full, kBoth);
-                mma_commit_pair(&bars.k_empty, kBoth);
                 // O = Q (R_hi + R_lo); the first MMA overwrites the accumulator
                 if (!w(&bars.rcopy, ph)) break;
                 if (c > 0 && !w(&bars.o_free, (c - 1) & 1)) break;
@@ -264,16 +313,15 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                         mma_pair(tmem + kTO, qa, dRlo + ro, id_q, 1);
                     }
                 mma_commit_pair(&bars.q_empty, kBoth);
-                // R += K^T Vz (R was rescaled by g^B with the copy)
-                if (!w(&bars.kt_full, ph) || !w(&bars.vz_ready, ph)) break;
+                // R += K^T Vz (R was rescaled by g^B with the copy), key block 0 then 1
+                if (!w(&bars.vz_ready, ph) || !w(&bars.kt_full0, ph)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const uint64_t ka = (uint64_t)(((t >> 3) * 2 * kBox + (t & 7) * 2048) >> 4);
-                    const uint64_t off = (uint64_t)((t * 2048) >> 4);
-                    mma_pair(tmem + kTR, dKT + ka, dV + off, id_r, 1);
-                }
-                mma_commit_pair(&bars.kt_empty, kBoth);
+                kv_block(0);
+                mma_commit_pair(&bars.kt_empty0, kBoth);
+                if (!w(&bars.kt_full1, ph)) break;
+                tc_fence_after();
+                kv_block(1);
+                mma_commit_pair(&bars.kt_empty1, kBoth);
                 mma_commit_pair(&bars.r_done, kBoth);
                 // O += (P_hi + P_lo) Vz
                 if (!w(&bars.p_ready, ph)) break;
@@ -294,7 +342,6 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
         }
     } else {
         // ------------------------------------------------------------ transform warps
-        const bool pwarp = warp < 6;                 // warps 2-5: scores + output; 6-9: state
         const int q4 = warp & 3;                     // TMEM lane quarter of this warp
         const int row = 32 * q4 + lane;              // TMEM lane
         const uint32_t lrow = (uint32_t)(32 * q4) << 16;
@@ -308,157 +355,17 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             if (!got) { ok = false; if (lane == 0) fail(); }
             return ok;
         };
+        // Every signal below publishes tensor memory (after tcgen05.fence::before_thread_sync)
+        // or shared memory that a proxy fence has made visible to the tensor cores that read
+        // it, so a CTA-scope release is enough; a cluster-scope one would also wait for the
+        // output warps' global stores to be acknowledged, which costs ~2 k cycles per chunk.
         auto arrive_lead = [&](uint64_t* bar) {
             __syncwarp();
-            if (lane == 0) mbar_arrive_cl(lead(bar));
+            if (lane == 0) mbar_arrive_remote(lead(bar));
         };
-        // output rows of chunk c: xi_j * O, straight from registers.  Each 128-byte row
-        // segment (32 fp32 or 64 bf16 columns = 8 items of 16 bytes) is transposed within
-        // 8-lane groups (8 consecutive rows), so that every store instruction writes four
-        // whole 128-byte segments.  The last TMEM read releases O for the next Q.R.
-        auto do_out = [&](int c) {
-            if (!wait(&bars.o_full, (uint32_t)c & 1u)) return;
-            tc_fence_after();
-            const float xi = exp2f(l2g * (float)(j + 1));
-            const int p8 = lane & 7;
-            const size_t row0 = (size_t)bh * N + (size_t)c * kB + (size_t)(j - p8);
-            constexpr int kSegs = OUT_BF16 ? 2 : 4;           // 128-byte segments per 128 columns
-            constexpr int kSegCols = OUT_BF16 ? 64 : 32;
-#pragma unroll 1
-            for (int sg = 0; sg < kSegs; ++sg) {
-                uint32_t a[8][4];
-                if (OUT_BF16) {
-                    float o[64];
-                    tmem_ld32(tmem + lrow + kTO + 64 * sg, o);
-                    tmem_ld32(tmem + lrow + kTO + 64 * sg + 32, o + 32);
-                    tmem_wait_ld();
-                    if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            a[k][w] = pack_bf16(xi * o[8 * k + 2 * w], xi * o[8 * k + 2 * w + 1]);
-                } else {
-                    float o[32];
-                    tmem_ld32(tmem + lrow + kTO + 32 * sg, o);
-                    tmem_wait_ld();
-                    if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
-                }
-                transpose8x8(a, p8);
-                const size_t col = (size_t)blk * 128 + (size_t)kSegCols * sg;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint4* dst;
-                    if (OUT_BF16)
-                        dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
-                                                       (row0 + k) * dv + col) + p8;
-                    else
-                        dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) + (row0 + k) * dv +
-                                                       col) + p8;
-                    *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
-                }
-            }
-        };
-        // State copy for chunk c: the hi/lo bf16 copy of R_{i-1} (this CTA's dk row j) and
-        // R <- g^B R in TMEM.  The 64 columns of the peer's block (remote half, warps 6-9)
-        // are transposed within 8-lane groups so that each remote store writes whole
-        // 128-byte rows of the peer's copy; the own 64 columns (warps 2-5) go to this CTA's
-        // copy.  R_{-1} comes from state_in (zero without it).
-        const float gB = dc.gB[head];
-        const uint32_t hi_peer = map_peer(rhi, peer);
-        const uint32_t lo_peer = map_peer(rlo, peer);
-        auto do_state = [&](int c, bool remote) {
-            if (c > 0) {
-                if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
-                tc_fence_after();
-            }
-            auto load = [&](int g, float* x) {
-                if (c == 0) {
-                    if (state_in) {
-                        const float4* src = reinterpret_cast<const float4*>(
-                            state_in + ((size_t)bh * kDk + j) * dv + blk * 128 + 32 * g);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float4 f = src[e];
-                            x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) x[e] = 0.f;
-                    }
-                } else {
-                    tmem_ld32(tmem + lrow + kTR + 32 * g, x);
-                    tmem_wait_ld();
-                }
-            };
-            auto rescale_store = [&](int g, float* x) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] *= gB;
-                tmem_st32(tmem + lrow + kTR + 32 * g, x);
-            };
-            if (remote) {
-                // both column groups in flight at once
-                const int g0 = 2 * (int)peer;
-                float x[64];
-                if (c == 0) {
-                    load(g0, x);
-                    load(g0 + 1, x + 32);
-                } else {
-                    tmem_ld32(tmem + lrow + kTR + 32 * g0, x);
-                    tmem_ld32(tmem + lrow + kTR + 32 * g0 + 32, x + 32);
-                    tmem_wait_ld();
-                }
-                uint32_t h[8][4], l[8][4];      // 16-byte chunks k = 8 columns each
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) split2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1], h[k][e], l[k][e]);
-                // the rescaled state goes back now (asynchronous until tcgen05.wait::st)
-                rescale_store(g0, x);
-                rescale_store(g0 + 1, x + 32);
-                // lane p of an 8-lane group then holds chunk p of row j0 + k in slot k
-                const int p8 = lane & 7;
-                const uint32_t j0 = (uint32_t)(j - p8);
-                transpose8x8(h, p8);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_cluster_v4(hi_peer + (j0 + k) * 128u + (((uint32_t)p8 ^ (uint32_t)k) << 4), h[k][0],
-                                  h[k][1], h[k][2], h[k][3]);
-                transpose8x8(l, p8);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_cluster_v4(lo_peer + (j0 + k) * 128u + (((uint32_t)p8 ^ (uint32_t)k) << 4), l[k][0],
-                                  l[k][1], l[k][2], l[k][3]);
-            } else {
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    const int g = 2 * (int)rank + half;
-                    float x[32];
-                    load(g, x);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t hh[4], ll[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split2(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1], hh[e], ll[e]);
-                        const uint32_t off = (uint32_t)j * 128u +
-                                             ((((uint32_t)(4 * half + cc)) ^ ((uint32_t)j & 7u)) << 4);
-                        *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                        *reinterpret_cast<uint4*>(rlo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-                    }
-                    rescale_store(g, x);
-                }
-            }
-            tmem_wait_st();
-            if (remote) fence_proxy_async_cluster(); else fence_proxy_async();
-            tc_fence_before();
-            arrive_lead(&bars.rcopy);
-        };
-        if (pwarp) {
+        if (warp < kFirstR) {
+            // -------------------------------------------------- scores -> P, then output
+            const int half = (warp - kFirstP) >> 2;  // key half (P) / 64-column half (O)
             const float cP = dc.cP[head];
             // P = g^(-B) S with the causal mask (key > j is zero), as hi/lo bf16 pairs in place.
             // Key quarter qq (32 keys) is below this warp's rows for qq < dq, holds their
@@ -478,81 +385,200 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     }
                 }
             };
-            if (nchunks > 0) do_state(0, false);
+            // output rows of chunk c: xi_j * O for this warp's 64 columns, straight from
+            // registers.  Each 128-byte row segment (32 fp32 or 64 bf16 columns = 8 items of
+            // 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so that every
+            // store instruction writes four whole 128-byte segments.  The last TMEM read
+            // releases O for the next Q.R.
+            const float xi = exp2f(l2g * (float)(j + 1));
+            auto do_out = [&](int c) {
+                if (!wait(&bars.o_full, (uint32_t)c & 1u)) return;
+                tc_fence_after();
+                const int p8 = lane & 7;
+                const size_t row0 = (size_t)bh * N + (size_t)c * kB + (size_t)(j - p8);
+                constexpr int kSegs = OUT_BF16 ? 1 : 2;           // 128-byte segments per 64 columns
+                constexpr int kSegCols = OUT_BF16 ? 64 : 32;
+#pragma unroll 1
+                for (int sg = 0; sg < kSegs; ++sg) {
+                    uint32_t a[8][4];
+                    const uint32_t tc0 = tmem + lrow + kTO + 64 * half + kSegCols * sg;
+                    if (OUT_BF16) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            float o[32];
+                            tmem_ld32(tc0 + 32 * hh, o);
+                            tmem_wait_ld();
+                            if (hh == 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                                for (int w = 0; w < 4; ++w)
+                                    a[4 * hh + k][w] =
+                                        pack_bf16(xi * o[8 * k + 2 * w], xi * o[8 * k + 2 * w + 1]);
+                        }
+                    } else {
+                        float o[32];
+                        tmem_ld32(tc0, o);
+                        tmem_wait_ld();
+                        if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
+                    }
+                    transpose8x8(a, p8);
+                    const size_t col = (size_t)blk * 128 + (size_t)(64 * half + kSegCols * sg);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint4* dst;
+                        if (OUT_BF16)
+                            dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
+                                                           (row0 + k) * dv + col) + p8;
+                        else
+                            dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) +
+                                                           (row0 + k) * dv + col) + p8;
+                        *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
+                    }
+                }
+            };
             for (int c = 0; c < nchunks && ok; ++c) {
                 if (!wait(&bars.s_full, (uint32_t)c & 1u)) break;
                 tc_fence_after();
-                // two quarters per step: both loads in flight before either is converted
 #pragma unroll 1
-                for (int qq = 0; qq <= dq; qq += 2) {
-                    const bool two = qq + 1 <= dq;
+                for (int qq = 4 * half; qq < 4 * half + 4; ++qq) {
                     const uint32_t ts = tmem + lrow + kTS + 32 * qq;
-                    float x[64];
                     uint32_t pp[32];
-                    tmem_ld32(ts, x);
-                    if (two) tmem_ld32(ts + 32, x + 32);
-                    tmem_wait_ld();
-                    convert(x, qq, pp);
-                    tmem_st32(ts, reinterpret_cast<const float*>(pp));
-                    if (two) {
-                        convert(x + 32, qq + 1, pp);
-                        tmem_st32(ts + 32, reinterpret_cast<const float*>(pp));
-                    }
-                }
-                {
-                    uint32_t zz[32];
+                    if (qq <= dq) {
+                        float x[32];
+                        tmem_ld32(ts, x);
+                        tmem_wait_ld();
+                        convert(x, qq, pp);
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) zz[e] = 0u;
-#pragma unroll 1
-                    for (int qq = dq + 1; qq < 8; ++qq)
-                        tmem_st32(tmem + lrow + kTS + 32 * qq, reinterpret_cast<const float*>(zz));
+                        for (int e = 0; e < 32; ++e) pp[e] = 0u;
+                    }
+                    tmem_st32(ts, reinterpret_cast<const float*>(pp));
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 arrive_lead(&bars.p_ready);
-                // while this chunk's last MMAs run: the own half of the next state copy
-                // (after K^T.Vz), then this chunk's output (after P.Vz)
-                if (c + 1 < nchunks) do_state(c + 1, false);
+                // while the chunk's P.Vz runs nothing is left to do; then its output
                 do_out(c);
             }
         } else {
-            // V rows kr = row and 128 + row of chunk c scaled in place by g^(B-1-kr); the
-            // block lands after the previous P.Vz, while this group copies the state
+            // -------------------------------------------------- state copy, then V -> Vz
+            const int g = warp - kFirstR;            // 0..7
+            const bool remote = g >= 4;              // peer's 64 columns (else this CTA's own)
+            const uint32_t cbase = 64u * (remote ? peer : rank);   // TMEM column of the 64
+            const float gB = dc.gB[head];
+            const uint32_t hi_peer = map_peer(rhi, peer);
+            const uint32_t lo_peer = map_peer(rlo, peer);
+            // State copy for chunk c: the hi/lo bf16 copy of R_{i-1} (this CTA's dk row j,
+            // 64 value columns) into the B operand of Q.R, and R <- g^B R in TMEM, in two
+            // halves of 32 columns (4 items of 16 bytes per row).  Own columns go to this
+            // CTA's copy; the peer's columns are transposed within 4-lane groups so that
+            // each remote store writes 64 contiguous bytes of a row of the peer's copy.
+            // R_{-1} comes from state_in (zero without it).
+            const int p4 = lane & 3;
+            const uint32_t j0 = (uint32_t)(j - p4);
+            auto do_state = [&](int c) {
+                if (c > 0) {
+                    if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
+                    tc_fence_after();
+                }
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t tcol = tmem + lrow + kTR + cbase + 32 * hh;
+                    float x[32];
+                    if (c == 0) {
+                        if (state_in) {
+                            const float4* src = reinterpret_cast<const float4*>(
+                                state_in + ((size_t)bh * kDk + j) * dv + blk * 128 + cbase + 32 * hh);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 f = src[e];
+                                x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) x[e] = 0.f;
+                        }
+                    } else {
+                        tmem_ld32(tcol, x);
+                        tmem_wait_ld();
+                    }
+                    uint32_t h[4][4], l[4][4];      // 16-byte items k = 8 columns each
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            split2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1], h[k][e], l[k][e]);
+                            x[8 * k + 2 * e] *= gB;
+                            x[8 * k + 2 * e + 1] *= gB;
+                        }
+                    // the rescaled state goes back now (asynchronous until tcgen05.wait::st)
+                    tmem_st32(tcol, x);
+                    if (remote) {
+                        // lane p of a 4-lane group then holds item 4hh+p of row j0 + k in slot k
+                        transpose4x4(h, p4);
+                        transpose4x4(l, p4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t r = j0 + (uint32_t)k;
+                            const uint32_t off =
+                                r * 128u + ((((uint32_t)(4 * hh + p4)) ^ (r & 7u)) << 4);
+                            st_cluster_v4(hi_peer + off, h[k][0], h[k][1], h[k][2], h[k][3]);
+                            st_cluster_v4(lo_peer + off, l[k][0], l[k][1], l[k][2], l[k][3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t off = (uint32_t)j * 128u +
+                                                 ((((uint32_t)(4 * hh + k)) ^ ((uint32_t)j & 7u)) << 4);
+                            *reinterpret_cast<uint4*>(rhi + off) = make_uint4(h[k][0], h[k][1], h[k][2], h[k][3]);
+                            *reinterpret_cast<uint4*>(rlo + off) = make_uint4(l[k][0], l[k][1], l[k][2], l[k][3]);
+                        }
+                    }
+                }
+                tmem_wait_st();
+                if (remote) fence_proxy_async_cluster(); else fence_proxy_async();
+                tc_fence_before();
+                arrive_lead(&bars.rcopy);
+            };
+            // V row kr of chunk c scaled in place by g^(B-1-kr); the block lands after the
+            // previous P.Vz, while this group copies the state
+            const int kr = 32 * g + lane;
+            const float fz = exp2f(l2g * (float)(kB - 1 - kr));
             auto do_v = [&](int c) {
                 if (!wait(&bars.v_full, (uint32_t)c & 1u)) return;
+                uint8_t* vrow = sv + kr * 128;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int kr = 128 * half + row;
-                    const float f = exp2f(l2g * (float)(kB - 1 - kr));
-                    uint8_t* vrow = sv + kr * 128;
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint4* pv = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
+                    uint4 u = *pv;
+                    uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint4* pv = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
-                        uint4 u = *pv;
-                        uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) wv[e] = pack_bf16(bf16_lo(wv[e]) * f, bf16_hi(wv[e]) * f);
-                        *pv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    }
+                    for (int e = 0; e < 4; ++e) wv[e] = pack_bf16(bf16_lo(wv[e]) * fz, bf16_hi(wv[e]) * fz);
+                    *pv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
                 fence_proxy_async();
                 arrive_lead(&bars.vz_ready);
             };
             for (int c = 0; c < nchunks && ok; ++c) {
-                do_state(c, true);
+                do_state(c);
                 do_v(c);
             }
-            // ---- final state: this CTA's dk rows of R_{N/B-1}
+            // ---- final state: this CTA's dk rows of R_{N/B-1}, this warp's 64 columns
             if (ok && state_out && nchunks > 0) {
                 if (wait(&bars.r_done, (uint32_t)(nchunks - 1) & 1u)) {
                     tc_fence_after();
 #pragma unroll 1
-                    for (int g = 0; g < 4; ++g) {
+                    for (int hh = 0; hh < 2; ++hh) {
                         float x[32];
-                        tmem_ld32(tmem + lrow + kTR + 32 * g, x);
+                        tmem_ld32(tmem + lrow + kTR + cbase + 32 * hh, x);
                         tmem_wait_ld();
                         float4* dst = reinterpret_cast<float4*>(
-                            state_out + ((size_t)bh * kDk + j) * dv + blk * 128 + 32 * g);
+                            state_out + ((size_t)bh * kDk + j) * dv + blk * 128 + cbase + 32 * hh);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);

@@ -328,6 +328,14 @@ __device__ __forceinline__ void mbar_arrive_cl(uint32_t bar_cl) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl)
                  : "memory");
 }
+// Arrive on a barrier given by its cluster address with the default (CTA-scope release)
+// semantics.  Enough when what the barrier publishes is tensor memory (ordered by
+// tcgen05.fence::before_thread_sync) or this SM's own shared memory made visible to its
+// tensor core by a proxy fence; it does not wait for the thread's earlier global stores
+// to be acknowledged, which a cluster-scope release does.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cl) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -376,6 +384,24 @@ __device__ __forceinline__ void transpose8x8(uint32_t (&a)[8][4], int p8) {
         const bool up = (p8 & m) != 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
+            if (k & m) continue;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t x = __shfl_xor_sync(0xffffffffu, up ? a[k][w] : a[k | m][w], m);
+                if (up) a[k][w] = x; else a[k | m][w] = x;
+            }
+        }
+    }
+}
+
+// The same for the 4 x 4 grid of 16-byte items held by each group of 4 lanes (two
+// butterfly stages over lane bits 0-1).
+__device__ __forceinline__ void transpose4x4(uint32_t (&a)[4][4], int p4) {
+#pragma unroll
+    for (int m = 1; m < 4; m <<= 1) {
+        const bool up = (p4 & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
             if (k & m) continue;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {

@@ -94,3 +94,24 @@ def test_streamed_rejects_segment_not_multiple_of_chunk():
     with pytest.raises(rb.RetentionError) as ei:
         rb.retention_chunkwise_host(hq, hk, hv, [0.9], 128, ho, 192)
     assert ei.value.status == rb.RET_ERR_SHAPE
+
+
+def test_owned_workspace_outlives_a_non_current_stream():
+    """The binding allocates the workspace on the current stream while the copies and
+    kernels run on `stream` and the copy streams: memory allocated (and overwritten) on the
+    current stream right after the call must not be the workspace block still in use."""
+    b, H, N, dk, dv, chunk, seg = 1, 4, 4096, 256, 512, 256, 1024
+    hq, hk, hv = host_qkv(b, H, N, dk, dv, 8300)
+    g = inputs.gammas(H)
+    nbytes = rb.chunkwise_host_workspace_bytes(hq.dtype, torch.float32, b, H, dk, dv, seg)
+    s = torch.cuda.Stream()
+    ho = torch.empty((b, H, N, dv), dtype=torch.float32, pin_memory=True)
+    rb.retention_chunkwise_host(hq, hk, hv, g, chunk, ho, seg, stream=s)
+    junk = [torch.full((nbytes // 4 + 1,), float("nan"), device=DEV) for _ in range(3)]
+    s.synchronize()
+    torch.cuda.synchronize()
+    del junk
+    assert not torch.isnan(ho).any()
+    one = rb.retention_chunkwise(hq.to(DEV), hk.to(DEV), hv.to(DEV), g, chunk).cpu()
+    assert err_f32(ho, one) < 1e-5
+    rb.check_device_error()

@@ -1,10 +1,17 @@
 """retention_chunkwise_host_noalloc: the host-streamed chunkwise call on the library's
 static device scratch instead of a caller workspace.
 
+The entry point is for callers that cannot call cudaMalloc: code hosted inside a framework
+whose caching allocator has already reserved the device memory (a cudaMalloc behind its back
+can fail with out-of-memory, or fragment the framework's pool), and latency-critical loops
+where cudaMalloc/cudaFree would synchronise the device.  They pass only inputs and outputs.
+
 Host-side checks (no GPU): the entry is exported, the scratch size is reported, and a
 call whose workspace would not fit, or with a bad segment length, is rejected before any
-device access.  On a GPU: the result equals retention_chunkwise_host with a caller
-workspace, and the final state is handed back.
+device access.  On a GPU: two calls in a row each equal retention_chunkwise_host with a
+caller workspace and the fp64 oracle (the scratch keeps the previous call's contents, so
+the second call checks that nothing stale leaks into it), and the final state is handed
+back.  This file is collected last so that a failure here leaves every other test run.
 """
 import ctypes
 
@@ -51,22 +58,31 @@ def test_rejections_before_any_device_access(L):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_caller_workspace():
+def test_noalloc_matches_caller_workspace_twice():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
+    import oracle
+    from _util import TOL_BF16, err_bf16
     b, H, N, dk, dv, chunk, seg = 1, 4, 1024, 256, 256, 256, 256
     assert rb.chunkwise_host_workspace_bytes(torch.bfloat16, torch.float32, b, H, dk, dv,
                                              seg) <= rb.chunkwise_host_static_scratch_bytes()
-    q, k, v = (inputs.randn((b, H, N, d), 9100 + i, 1 / 16, "bf16", "cpu").pin_memory()
-               for i, d in enumerate((dk, dk, dv)))
     g = inputs.gammas(H)
-    s0 = inputs.randn((b, H, dk, dv), 9110, 0.05, "f32", "cuda")
-    o1 = torch.empty((b, H, N, dv), dtype=torch.float32, pin_memory=True)
-    o2 = torch.empty_like(o1, pin_memory=True)
-    s1, s2 = s0.clone(), s0.clone()
-    rb.retention_chunkwise_host(q, k, v, g, chunk, o1, seg, state_in=s1, state_out=s1)
-    rb.retention_chunkwise_host_noalloc(q, k, v, g, chunk, o2, seg, state_in=s2, state_out=s2)
-    torch.cuda.synchronize()
-    assert torch.equal(o1, o2)
-    assert torch.equal(s1, s2)
+    for call_no in range(2):
+        base = 9100 + 10 * call_no
+        q, k, v = (inputs.randn((b, H, N, d), base + i, 1 / 16, "bf16", "cpu").pin_memory()
+                   for i, d in enumerate((dk, dk, dv)))
+        s0 = inputs.randn((b, H, dk, dv), base + 5, 0.05, "f32", "cuda")
+        o1 = torch.empty((b, H, N, dv), dtype=torch.float32, pin_memory=True)
+        o2 = torch.empty_like(o1, pin_memory=True)
+        o2.fill_(float("nan"))
+        s1, s2 = s0.clone(), s0.clone()
+        rb.retention_chunkwise_host(q, k, v, g, chunk, o1, seg, state_in=s1, state_out=s1)
+        rb.retention_chunkwise_host_noalloc(q, k, v, g, chunk, o2, seg, state_in=s2,
+                                            state_out=s2)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2), f"call {call_no}"
+        assert torch.equal(s1, s2), f"call {call_no}"
+        want, want_state = oracle.chunkwise(q, k, v, g, chunk, state_in=s0, return_state=True)
+        assert err_bf16(o2, want) < TOL_BF16, f"call {call_no}"
+        assert err_bf16(s2, want_state) < TOL_BF16, f"call {call_no}"
     rb.check_device_error()
