@@ -289,6 +289,17 @@ const char* retention_status_string(int status);
 int retention_check_device_error(void* stream);
 
 /*
+ * Diagnostics of the tensor-core chunkwise kernel for chunk 256, dk 256 (pairs of SMs):
+ * it computes the score x value and query x state products with fp16 operands and, if a
+ * value it rounds to fp16 lies outside fp16's range (|x| >= 65504), re-runs that unit
+ * (one batch x head x 128 value columns) in a bf16 hi/lo format with fp32's range, inside
+ * the same launch; the result is correct either way.  This call synchronises `stream` and
+ * returns the number of such re-runs since the previous call (and resets the count), or
+ * -1 if the synchronisation failed.  Host-side; for tests and diagnostics.
+ */
+int retention_chunkwise_format_reruns(void* stream);
+
+/*
  * Number of kernels this library has launched in this process so far (all
  * devices, all calls).  Host-side counter, incremented after each successful
  * launch; lets callers count launches inside a timed region.

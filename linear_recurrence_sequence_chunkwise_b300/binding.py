@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.retention_status_string.argtypes = [i]
             L.retention_status_string.restype = ctypes.c_char_p
             L.retention_check_device_error.argtypes = [vp]
+            L.retention_chunkwise_format_reruns.argtypes = [vp]
+            L.retention_chunkwise_format_reruns.restype = ctypes.c_int
             L.retention_kernel_launches.argtypes = []
             L.retention_kernel_launches.restype = ctypes.c_ulonglong
             L.retention_last_kernel.argtypes = []
@@ -381,6 +383,15 @@ def kernel_launches() -> int:
 def last_kernel() -> str:
     """Name of the kernel this host thread launched last (see RET_KERNEL_* codes)."""
     return KERNEL_NAMES.get(int(lib().retention_last_kernel()), "unknown")
+
+
+def chunkwise_format_reruns(stream=None) -> int:
+    """Synchronise and return (and reset) how many units of the pair-of-SMs chunkwise kernel
+    re-ran in the bf16 hi/lo format because an fp16 operand left fp16's range."""
+    n = int(lib().retention_chunkwise_format_reruns(_stream(stream)))
+    if n < 0:
+        raise RetentionError("retention_chunkwise_format_reruns", RET_ERR_CUDA, "sync failed")
+    return n
 
 
 def check_device_error(stream=None):

@@ -121,5 +121,7 @@ int record_cuda_status(cudaError_t e);
 // Device error words of the kernels with bounded waits: read and clear.
 unsigned read_clear_error_tc_chunkwise(cudaStream_t s);
 unsigned read_clear_error_tc_chunkwise_pair(cudaStream_t s);
+// Units of the pair chunkwise kernel that re-ran in the hi/lo bf16 format: read and clear.
+unsigned read_clear_reruns_tc_chunkwise_pair(cudaStream_t s);
 unsigned read_clear_error_tc_parallel(cudaStream_t s);
 }  // namespace ret

@@ -312,6 +312,12 @@ const char* retention_cuda_error_string(int cuda_error) {
     return buf;
 }
 
+int retention_chunkwise_format_reruns(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+    return (int)ret::read_clear_reruns_tc_chunkwise_pair(s);
+}
+
 int retention_check_device_error(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce = cudaStreamSynchronize(s);

@@ -5,59 +5,82 @@
 //     O[iB+j] = sum_{r<=j} (q_j.k_r) g^(j-r) v_r + g^(j+1) (q_j R_{i-1})
 //     R_i     = sum_r g^(B-1-r) k_r^T v_r + g^B R_{i-1}
 // for bf16 Q/K/V, fp32 accumulation and state, chunk B = 256, dk = 256, dv a multiple of
-// 128.  Decay folding and the hi/lo bf16 split of the state copy and of the scores are
-// those of tc_chunkwise.cu (Vz = zeta (.) V, P = g^(-B) S (.) M, xi_j applied to the
-// output rows, R <- g^B R then R += K^T Vz).
+// 128.
+//
+// Decay folding (no per-element power): V rows are scaled by zeta_r = g^(B-1-r) (Vz), the
+// scores by the constant a = g^(-B/2) with the causal mask (P = a S (.) M), the state copy
+// that Q multiplies by c = g^(B/2) (R' = c R), and each output row by xi_j = g^(j+1-B/2):
+//     xi_j (P Vz + Q R')_j = sum_{r<=j} S_jr g^(j-r) v_r + g^(j+1) q_j R.
+// The state update is R <- g^B R (one TMEM pass per chunk), then R += K^T Vz.  Splitting
+// g^(-B) evenly between a and xi keeps both within g^(-B/2).
+//
+// Operand formats.  S = Q K^T and R += K^T Vz take bf16 operands as loaded (exact products).
+// The two products whose operands are computed take fp16 (11 significant bits, 8x finer
+// than bf16): O += P Vz16 with P and Vz16 = fp16(Vz), and O = Q16 R'16 with Q converted to
+// fp16 in shared memory once S has read it (bf16 -> fp16 is exact in fp16's normal range)
+// and R'16 = fp16(c R).  A CPU emulation of these rounding points on the long-sequence
+// workload (heads 0, 5, 15) gives max errors of 0.009, 0.009 and 0.002 of the head's RMS,
+// against 0.013, 0.009 and 0.001 for bf16 hi/lo pairs of P and R' (two MMAs each).
+// fp16 holds |x| < 65504 only: every conversion tracks the largest magnitude it rounds,
+// and if any exceeds the range the pair re-runs its whole unit (same kernel, second pass)
+// with the hi/lo bf16 pairs instead, which have fp32's range.  The host picks the hi/lo
+// format from the start when g^(-B) > 4096 for some head (small decays underflow Vz16).
 //
 // Work split: one cluster of two CTAs (the two SMs of a pair) per (batch*head, 128-column
 // block of dv); the even CTA issues every MMA as a pair MMA (M = 256, 128 rows per SM):
 //   S  = Q K^T        M = 256 query rows of the chunk (CTA r: rows 128r..), N = 256 keys
 //                     (B operand split: CTA r holds keys 128r..), K = dk
-//   O  = Q R_{i-1}    N = 128 value columns (B split: CTA r holds the bf16 hi/lo copy of
-//                     R[:, 64r..64r+63]), K = dk, as two MMAs (hi, lo)
+//   O  = Q R'         N = 128 value columns (B split: CTA r holds the copy of
+//                     R'[:, 64r..64r+63]), K = dk (fp16: one MMA per K step; hi/lo: two)
 //   R += K^T Vz       M = 256 dk rows (CTA r: dk 128r..; the state lives in tensor memory,
 //                     split by dk), N = 128 value columns, K = 256 keys
-//   O += P Vz         A = P from tensor memory (hi and lo), N = 128, K = 256 keys
-// Every MMA has N >= 128 per SM, and each SM reads only its half of each B operand, so
-// the tensor pipe runs at full rate with half the shared-memory operand traffic of the
-// one-SM split into 64-column blocks, and the score tile of a head is computed by dv/128
-// pairs instead of dv/64 CTAs.  The pair costs one duplicated quarter of the score tile
-// (the even CTA's rows against keys 128-255, all masked) and of P.V.
+//   O += P Vz         A = P from tensor memory, N = 128, K = 256 keys
+// Every MMA has N >= 128 per SM, and each SM reads only its half of each B operand.  The
+// pair costs one duplicated quarter of the score tile (the even CTA's rows against keys
+// 128-255, all masked) and of P.V.
 //
-// Roles (576 threads = 18 warps per CTA).  The transform work of a chunk is spread over
-// sixteen warps in two groups that run side by side, so that no group has more than one
-// task on the path between two MMAs:
+// Roles (576 threads = 18 warps per CTA):
 //   warp 0      TMA loads of this CTA (Q, K and the K^T operand complete on the even CTA's
 //               barriers, V on a local one) and L2 prefetches one chunk ahead
 //   warp 1      tensor-memory allocation (both CTAs, collectively); in the even CTA the
 //               MMA issuer
-//   warps 2-9   scores -> P (two warps per TMEM lane quarter, one per 128-key half), then
-//               the chunk's output rows (one per 64-column half), coalesced stores
-//   warps 10-17 state copy (two warps per lane quarter: this CTA's own 64 value columns
-//               into its own shared memory, the peer's 64 into the peer's, 64-byte row
-//               pieces), the rescale
-//               R <- g^B R, then V -> Vz (one key row per thread)
+//   warps 2-9   V -> Vz and Vz16 (one key row per thread), then scores -> P (two warps per
+//               TMEM lane quarter, one per 128-key half), then the chunk's output rows
+//               (one per 64-column half), coalesced stores
+//   warps 10-17 state copy (10-13 this CTA's own 64 value columns, 14-17 the peer's, into
+//               the peer's shared memory in 64-byte row pieces) with R <- g^B R, then
+//               Q -> fp16 in place (one row of one dk box per thread: dk 0-127 after S's
+//               first half, dk 128-255 after its second)
 // Warp w reaches TMEM lanes 32*(w%4)..+31.  Every wait is bounded; a wait that gives up
 // sets the device error word and both CTAs' abort flags, and the CTAs unwind, meet at a
-// final cluster barrier and free their tensor memory.
+// final cluster barrier and free their tensor memory.  Warp signals use CTA-scope release
+// arrives: each publishes tensor memory (after tcgen05.fence::before_thread_sync) or shared
+// memory that a proxy fence has made visible to the tensor cores reading it; a cluster-scope
+// release would also wait for the output warps' global stores to be acknowledged.
 //
 // Tensor memory per CTA (512 columns x 128 lanes, fp32):
-//   [  0,256) S: this CTA's 128 query rows x 256 keys; P written in place as bf16 pairs
-//             (per 32 keys: 16 columns of hi pairs, then 16 of lo pairs)
+//   [  0,256) S: this CTA's 128 query rows x 256 keys; P written in place, per 32 keys
+//             (32 columns of S): fp16 pairs in the first 16 columns (hi/lo format: bf16 hi
+//             pairs in the first 16, lo pairs in the next 16)
 //   [256,384) O: this CTA's 128 query rows x 128 value columns
 //   [384,512) R: this CTA's 128 dk rows of the state x 128 value columns
-// Shared memory per CTA (1024-aligned, 224 KB), each box 128 rows x 64 bf16, 128B swizzle:
-//   Q   64 KB  own 128 query rows x 4 dk boxes
-//   K   64 KB  own 128 keys x 4 dk boxes (S); after S the K^T operand of the state update:
-//              key block j (keys 128j..) x own 128 dk columns in boxes 2j, 2j+1.  The own
-//              key block's boxes stay from S; the peer key block is loaded into the two
-//              boxes S no longer needs (the same offsets in both CTAs)
-//   V   32 KB  256 keys x own 64 value columns (scaled in place to Vz)
-//   Rhi 32 KB, Rlo 32 KB  bf16 copy of R_{i-1}: 256 dk rows x own 64 columns
-// MMA order in a chunk: S (dk boxes 0-1, then 2-3), Q.R, K^T.Vz (key block 0, then 1),
-// P.Vz.  Commits between the halves free shared memory early: after S's first half the
-// odd CTA loads its peer key block (boxes 0-1), after its second half the even CTA
-// (boxes 2-3); after K^T.Vz's first half the next chunk's keys load into boxes 0-1.
+// Shared memory per CTA (1024-aligned, 224 KB), each box 128 rows x 64 16-bit values, 128B
+// swizzle:
+//   Q    64 KB  own 128 query rows x 4 dk boxes (bf16 for S, then fp16 for Q.R)
+//   K    64 KB  own 128 keys x 4 dk boxes (S); after S the K^T operand of the state update:
+//               key block j (keys 128j..) x own 128 dk columns in boxes 2j, 2j+1.  The own
+//               key block's boxes stay from S; the peer key block is loaded into the two
+//               boxes S no longer needs (the same offsets in both CTAs)
+//   V    32 KB  256 keys x own 64 value columns (scaled in place to bf16 Vz)
+//   V16  32 KB  fp16 Vz (hi/lo format: the lo part of R')
+//   R16  32 KB  fp16 R' = c R_{i-1}: 256 dk rows x own 64 columns (hi/lo format: hi part)
+// MMA order in a chunk: S (dk boxes 0-1, then 2-3), Q.R' (dk 0-127, then 128-255), K^T.Vz
+// (key block 0, then 1), P.Vz.  Commits between the halves free shared memory early:
+// after S's first half the odd CTA loads its peer key block (boxes 0-1) and Q's first half
+// is converted, after its second half the even CTA loads (boxes 2-3); after K^T.Vz's first
+// half the next chunk's keys load into boxes 0-1.
+#include <type_traits>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
@@ -66,35 +89,40 @@ namespace ret {
 namespace {
 
 __device__ unsigned g_err_chunkwise_pair;
+__device__ unsigned g_reruns_chunkwise_pair;   // units re-run in the hi/lo bf16 format
 
 using namespace tc;
 
 constexpr int kThreads = 576;
 constexpr int kB = 256;                        // chunk length
 constexpr int kDk = 256;
-constexpr int kBox = 128 * 128;                // 128 rows x 64 bf16
+constexpr int kBox = 128 * 128;                // 128 rows x 64 16-bit values
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + 4 * kBox;
 constexpr int kVOff = kKOff + 4 * kBox;
-constexpr int kRhiOff = kVOff + 2 * kBox;
-constexpr int kRloOff = kRhiOff + 2 * kBox;
-constexpr int kSmemBytes = kRloOff + 2 * kBox;  // 229376
+constexpr int kV16Off = kVOff + 2 * kBox;
+constexpr int kR16Off = kV16Off + 2 * kBox;
+constexpr int kSmemBytes = kR16Off + 2 * kBox;  // 229376
 constexpr uint32_t kTS = 0, kTO = 256, kTR = 384;
 constexpr uint32_t kPairArrivals = 16;         // 8 warps in each CTA
 constexpr uint16_t kBoth = 3;                  // multicast mask: both CTAs of the pair
 constexpr int kFirstP = 2, kFirstR = 10;       // first warp of each transform group
+constexpr float kF16Max = 65504.0f;
 
 struct Decay {
     float l2g[kMaxHeads];   // log2(gamma)
     float gB[kMaxHeads];    // gamma^B
-    float cP[kMaxHeads];    // gamma^(-B)
+    float a[kMaxHeads];     // gamma^(-B/2): score scale
+    float c[kMaxHeads];     // gamma^(B/2): state-copy scale
 };
 
 struct Bars {
     // the even CTA's copies count both CTAs' work
     uint64_t q_full, k_full0, k_full1;             // pair loads: Q; K dk boxes 0-1 / 2-3
     uint64_t kt_full0, kt_full1;                   // peer key block of K^T in boxes 0-1 / 2-3
-    uint64_t vz_ready, p_ready, rcopy, o_free;     // warp arrivals of both CTAs
+    uint64_t vz_ready, p_ready, o_free;            // warp arrivals of both CTAs
+    uint64_t rcopy;                                // state copy, 8 warps of each CTA
+    uint64_t q16_0, q16_1;                         // Q halves in fp16, 8 warps of each CTA
 
     // each CTA's own copy, arrived on by the MMA commits (multicast)
     uint64_t q_empty;                              // Q.R done: Q area free
@@ -107,6 +135,10 @@ struct Bars {
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+    __half2 t = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
 }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -122,17 +154,18 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                       const __grid_constant__ CUtensorMap mv,
                       void* __restrict__ out_base, const float* __restrict__ state_in,
                       float* __restrict__ state_out, int N,
-                      int H, int dv, const Decay dc) {
+                      int H, int dv, int fp16_first, const Decay dc) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = sm + kQOff;
     uint8_t* sk = sm + kKOff;
     uint8_t* sv = sm + kVOff;
-    uint8_t* rhi = sm + kRhiOff;
-    uint8_t* rlo = sm + kRloOff;
+    uint8_t* sv16 = sm + kV16Off;
+    uint8_t* sr16 = sm + kR16Off;
     __shared__ Bars bars;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ int range_flag;                   // an fp16 conversion left fp16's range
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -143,13 +176,16 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
     const int head = bh % H;
     const int nchunks = N / kB;
     volatile int* abort_p = &abort_flag;
+    volatile int* range_p = &range_flag;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        range_flag = 0;
         mbar_init(&bars.q_full, 1); mbar_init(&bars.k_full0, 1); mbar_init(&bars.k_full1, 1);
         mbar_init(&bars.kt_full0, 1); mbar_init(&bars.kt_full1, 1);
         mbar_init(&bars.vz_ready, kPairArrivals); mbar_init(&bars.p_ready, kPairArrivals);
-        mbar_init(&bars.rcopy, kPairArrivals); mbar_init(&bars.o_free, kPairArrivals);
+        mbar_init(&bars.o_free, kPairArrivals); mbar_init(&bars.rcopy, kPairArrivals);
+        mbar_init(&bars.q16_0, kPairArrivals); mbar_init(&bars.q16_1, kPairArrivals);
         mbar_init(&bars.q_empty, 1); mbar_init(&bars.s_half, 1); mbar_init(&bars.s_full, 1);
         mbar_init(&bars.kt_empty0, 1); mbar_init(&bars.kt_empty1, 1);
         mbar_init(&bars.v_empty, 1); mbar_init(&bars.o_full, 1); mbar_init(&bars.r_done, 1);
@@ -162,332 +198,398 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     const uint32_t peer_abort = map_peer(&abort_flag, peer);
+    const uint32_t peer_range = map_peer(&range_flag, peer);
     auto fail = [&]() {
         *abort_p = 1;
         st_cluster_s32(peer_abort, 1);
         atomicOr(&g_err_chunkwise_pair, 1u);
     };
     auto lead = [&](uint64_t* b) { return map_peer(b, 0); };
+    // a conversion to fp16 met a magnitude outside fp16's range: both CTAs re-run the unit
+    auto out_of_range = [&](float m) {
+        if (!(m < kF16Max)) {       // also catches NaN
+            *range_p = 1;
+            st_cluster_s32(peer_range, 1);
+        }
+    };
+    uint32_t drains = 0;             // MMA drains waited for (MMA issuer)
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv);
-            const uint32_t qf = lead(&bars.q_full), kf0 = lead(&bars.k_full0),
-                           kf1 = lead(&bars.k_full1);
-            const uint32_t ktf = lead(rank == 0 ? &bars.kt_full1 : &bars.kt_full0);
-            const int rowbase = bh * N;
-            const int own = 128 * (int)rank, other = 128 * (int)peer;
-            const int vcol = blk * 128 + 64 * (int)rank;
-            uint32_t armed_q = 0, armed_k = 0, armed_kt = 0, v_loads = 0;
-            bool ok = true;
-            auto w = [&](uint64_t* bar, uint32_t par) {
-                if (ok && !mbar_wait(bar, par, abort_p)) { ok = false; fail(); }
-                return ok;
-            };
-            // the pairs of one head share Q and K: pull the next chunk's boxes into L2
-            auto prefetch = [&](int c) {
-                if (c >= nchunks) return;
-                const int r0 = rowbase + c * kB;
-                for (int a = 0; a < 4; ++a) {
-                    tma_prefetch_l2(&mq, 64 * a, r0 + own);
-                    tma_prefetch_l2(&mk, 64 * a, r0 + own);
-                }
-                for (int m = 0; m < 2; ++m) tma_prefetch_l2(&mk, 64 * (2 * (int)rank + m), r0 + other);
-                for (int j = 0; j < 2; ++j) tma_prefetch_l2(&mv, vcol, r0 + 128 * j);
-            };
-            prefetch(0);
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const uint32_t pp = (uint32_t)(c - 1) & 1u;
-                const int r0 = rowbase + c * kB;
-                // Q: own query rows, all dk (after the previous chunk's Q.R)
-                if (c > 0 && !w(&bars.q_empty, pp)) break;
-                if (rank == 0) { mbar_arrive_expect_tx(&bars.q_full, 2 * 4 * kBox); ++armed_q; }
-                for (int a = 0; a < 4; ++a) tma_load_2d_pair(sq + a * kBox, &mq, 64 * a, r0 + own, qf);
-                // K: own keys; dk boxes 0-1 once K^T.Vz has read key block 0, boxes 2-3 once
-                // it has read key block 1
-                if (c > 0 && !w(&bars.kt_empty0, pp)) break;
-                if (rank == 0) {
-                    mbar_arrive_expect_tx(&bars.k_full0, 2 * 2 * kBox);
-                    mbar_arrive_expect_tx(&bars.k_full1, 2 * 2 * kBox);
-                    ++armed_k;
-                }
-                for (int a = 0; a < 2; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf0);
-                if (c > 0 && !w(&bars.kt_empty1, pp)) break;
-                for (int a = 2; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf1);
-                // V: all keys of the chunk, own 64 value columns (after the previous P.Vz)
-                if (c > 0 && !w(&bars.v_empty, pp)) break;
-                mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
-                for (int j = 0; j < 2; ++j) tma_load_2d(sv + j * kBox, &mv, vcol, r0 + 128 * j, &bars.v_full);
-                ++v_loads;
-                // K^T operand of the state update: the peer key block x own dk half goes
-                // into boxes 2*peer, 2*peer+1 once S has read them (the odd CTA's after S's
-                // first half, the even CTA's after all of S)
-                if (!w(rank == 1 ? &bars.s_half : &bars.s_full, (uint32_t)c & 1u)) break;
-                if (rank == 0) {
-                    mbar_arrive_expect_tx(&bars.kt_full0, 2 * kBox);
-                    mbar_arrive_expect_tx(&bars.kt_full1, 2 * kBox);
-                    ++armed_kt;
-                }
-                for (int m = 0; m < 2; ++m)
-                    tma_load_2d_pair(sk + (2 * (int)peer + m) * kBox, &mk, 64 * (2 * (int)rank + m),
-                                     r0 + other, ktf);
-                // the next chunk's boxes into L2, behind this chunk's loads in the TMA queue
-                prefetch(c + 1);
-            }
-            if (!ok) {
-                // let loads in flight land before the CTAs unwind
-                if (v_loads) mbar_wait(&bars.v_full, (v_loads - 1) & 1, nullptr, 100000000ull);
-                if (rank == 0) {
-                    if (armed_q) mbar_wait(&bars.q_full, (armed_q - 1) & 1, nullptr, 100000000ull);
-                    if (armed_k) {
-                        mbar_wait(&bars.k_full0, (armed_k - 1) & 1, nullptr, 100000000ull);
-                        mbar_wait(&bars.k_full1, (armed_k - 1) & 1, nullptr, 100000000ull);
-                    }
-                    if (armed_kt) {
-                        mbar_wait(&bars.kt_full0, (armed_kt - 1) & 1, nullptr, 100000000ull);
-                        mbar_wait(&bars.kt_full1, (armed_kt - 1) & 1, nullptr, 100000000ull);
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (even CTA)
-        if (rank == 0 && lane == 0) {
-            const uint32_t id_s = idesc_bf16(256, 256, 0, 0);    // Q K^T: both K-major
-            const uint32_t id_q = idesc_bf16(256, 128, 0, 1);    // Q R: B MN-major
-            const uint32_t id_r = idesc_bf16(256, 128, 1, 1);    // K^T Vz: both MN-major
-            const uint32_t id_p = idesc_bf16(256, 128, 0, 1);    // P Vz: A in TMEM, B MN-major
-            // descriptors are linear in the start address: base descriptor + offset / 16
-            const uint64_t dQ = sdesc_sw128(smem_u32(sq), 16, 1024);
-            const uint64_t dK = sdesc_sw128(smem_u32(sk), 16, 1024);
-            const uint64_t dKT = sdesc_sw128(smem_u32(sk), kBox, 1024);   // dk boxes 16 KB apart
-            const uint64_t dV = sdesc_sw128(smem_u32(sv), 2 * kBox, 1024);
-            const uint64_t dRhi = sdesc_sw128(smem_u32(rhi), 2 * kBox, 1024);
-            const uint64_t dRlo = sdesc_sw128(smem_u32(rlo), 2 * kBox, 1024);
-            bool ok = true;
-            auto w = [&](uint64_t* bar, uint32_t par) {
-                if (ok && !mbar_wait_cl(bar, par, abort_p)) { ok = false; fail(); }
-                return ok;
-            };
-            auto s_boxes = [&](int a0) {
+    // Pass 0 uses the fp16 format (unless the host chose hi/lo); pass 1 runs only if pass 0
+    // left fp16's range somewhere in this pair's unit, and recomputes it with hi/lo pairs.
 #pragma unroll 1
-                for (int a = a0; a < a0 + 2; ++a)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t off = (uint64_t)((a * kBox + kk * 32) >> 4);
-                        mma_pair(tmem + kTS, dQ + off, dK + off, id_s, (a | kk) != 0);
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool f16 = fp16_first && pass == 0;
+        const int base = pass * nchunks;               // phase index of chunk 0 of this pass
+        auto par = [&](int c) { return (uint32_t)(base + c) & 1u; };
+
+        if (warp == 0) {
+            // -------------------------------------------------------- TMA producer
+            if (lane == 0) {
+                if (pass == 0) { tma_prefetch_desc(&mq); tma_prefetch_desc(&mk); tma_prefetch_desc(&mv); }
+                const uint32_t qf = lead(&bars.q_full), kf0 = lead(&bars.k_full0),
+                               kf1 = lead(&bars.k_full1);
+                const uint32_t ktf = lead(rank == 0 ? &bars.kt_full1 : &bars.kt_full0);
+                const int rowbase = bh * N;
+                const int own = 128 * (int)rank, other = 128 * (int)peer;
+                const int vcol = blk * 128 + 64 * (int)rank;
+                uint32_t armed_q = 0, armed_k = 0, armed_kt = 0, v_loads = 0;
+                bool ok = !*abort_p;
+                auto w = [&](uint64_t* bar, uint32_t p) {
+                    if (ok && !mbar_wait(bar, p, abort_p)) { ok = false; fail(); }
+                    return ok;
+                };
+                // the pairs of one head share Q and K: pull the next chunk's boxes into L2
+                auto prefetch = [&](int c) {
+                    if (c >= nchunks) return;
+                    const int r0 = rowbase + c * kB;
+                    for (int a = 0; a < 4; ++a) {
+                        tma_prefetch_l2(&mq, 64 * a, r0 + own);
+                        tma_prefetch_l2(&mk, 64 * a, r0 + own);
                     }
-            };
-            auto kv_block = [&](int j) {
-#pragma unroll
-                for (int t = 8 * j; t < 8 * j + 8; ++t) {
-                    const uint64_t ka = (uint64_t)(((t >> 3) * 2 * kBox + (t & 7) * 2048) >> 4);
-                    const uint64_t off = (uint64_t)((t * 2048) >> 4);
-                    mma_pair(tmem + kTR, dKT + ka, dV + off, id_r, 1);
-                }
-            };
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const uint32_t ph = (uint32_t)c & 1u;
-                // S = Q K^T (the previous P.Vz, issued earlier, reads the S columns first:
-                // tcgen05.mma operations of one thread run in issue order)
-                if (!w(&bars.q_full, ph) || !w(&bars.k_full0, ph)) break;
-                tc_fence_after();
-                s_boxes(0);
-                mma_commit_pair(&bars.s_half, kBoth);
-                if (!w(&bars.k_full1, ph)) break;
-                tc_fence_after();
-                s_boxes(2);
-                mma_commit_pair(&bars.s_full, kBoth);
-                // O = Q (R_hi + R_lo); the first MMA overwrites the accumulator
-                if (!w(&bars.rcopy, ph)) break;
-                if (c > 0 && !w(&bars.o_free, (c - 1) & 1)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t qa = dQ + (uint64_t)((a * kBox + kk * 32) >> 4);
-                        const uint64_t ro = (uint64_t)(((4 * a + kk) * 2048) >> 4);
-                        mma_pair(tmem + kTO, qa, dRhi + ro, id_q, (a | kk) != 0);
-                        mma_pair(tmem + kTO, qa, dRlo + ro, id_q, 1);
+                    for (int m = 0; m < 2; ++m) tma_prefetch_l2(&mk, 64 * (2 * (int)rank + m), r0 + other);
+                    for (int j = 0; j < 2; ++j) tma_prefetch_l2(&mv, vcol, r0 + 128 * j);
+                };
+                if (ok) prefetch(0);
+                for (int c = 0; c < nchunks && ok; ++c) {
+                    const int r0 = rowbase + c * kB;
+                    // Q: own query rows, all dk (after the previous chunk's Q.R)
+                    if (c > 0 && !w(&bars.q_empty, par(c - 1))) break;
+                    if (rank == 0) { mbar_arrive_expect_tx(&bars.q_full, 2 * 4 * kBox); ++armed_q; }
+                    for (int a = 0; a < 4; ++a) tma_load_2d_pair(sq + a * kBox, &mq, 64 * a, r0 + own, qf);
+                    // K: own keys; dk boxes 0-1 once K^T.Vz has read key block 0, boxes 2-3
+                    // once it has read key block 1
+                    if (c > 0 && !w(&bars.kt_empty0, par(c - 1))) break;
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(&bars.k_full0, 2 * 2 * kBox);
+                        mbar_arrive_expect_tx(&bars.k_full1, 2 * 2 * kBox);
+                        ++armed_k;
                     }
-                mma_commit_pair(&bars.q_empty, kBoth);
-                // R += K^T Vz (R was rescaled by g^B with the copy), key block 0 then 1
-                if (!w(&bars.vz_ready, ph) || !w(&bars.kt_full0, ph)) break;
-                tc_fence_after();
-                kv_block(0);
-                mma_commit_pair(&bars.kt_empty0, kBoth);
-                if (!w(&bars.kt_full1, ph)) break;
-                tc_fence_after();
-                kv_block(1);
-                mma_commit_pair(&bars.kt_empty1, kBoth);
-                mma_commit_pair(&bars.r_done, kBoth);
-                // O += (P_hi + P_lo) Vz
-                if (!w(&bars.p_ready, ph)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const uint32_t a_hi = tmem + kTS + 32 * (t >> 1) + 8 * (t & 1);
-                    const uint64_t bd = dV + (uint64_t)((t * 2048) >> 4);
-                    mma_pair_ts(tmem + kTO, a_hi, bd, id_p, 1);
-                    mma_pair_ts(tmem + kTO, a_hi + 16, bd, id_p, 1);
-                }
-                mma_commit_pair(&bars.o_full, kBoth);
-                mma_commit_pair(&bars.v_empty, kBoth);
-            }
-            // every issued MMA completes before tensor memory is released
-            mma_commit_pair(&bars.drain, 1);
-            mbar_wait(&bars.drain, 0, nullptr, 200000000ull);
-        }
-    } else {
-        // ------------------------------------------------------------ transform warps
-        const int q4 = warp & 3;                     // TMEM lane quarter of this warp
-        const int row = 32 * q4 + lane;              // TMEM lane
-        const uint32_t lrow = (uint32_t)(32 * q4) << 16;
-        const int j = 128 * (int)rank + row;         // query row in the chunk / dk row of R
-        const float l2g = dc.l2g[head];
-        bool ok = true;
-        // tcgen05.ld/st are warp-collective: keep the outcome of every wait uniform
-        auto wait = [&](uint64_t* bar, uint32_t par) {
-            if (!ok) return false;
-            const bool got = __all_sync(0xffffffffu, mbar_wait(bar, par, abort_p));
-            if (!got) { ok = false; if (lane == 0) fail(); }
-            return ok;
-        };
-        // Every signal below publishes tensor memory (after tcgen05.fence::before_thread_sync)
-        // or shared memory that a proxy fence has made visible to the tensor cores that read
-        // it, so a CTA-scope release is enough; a cluster-scope one would also wait for the
-        // output warps' global stores to be acknowledged, which costs ~2 k cycles per chunk.
-        auto arrive_lead = [&](uint64_t* bar) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(lead(bar));
-        };
-        if (warp < kFirstR) {
-            // -------------------------------------------------- scores -> P, then output
-            const int half = (warp - kFirstP) >> 2;  // key half (P) / 64-column half (O)
-            const float cP = dc.cP[head];
-            // P = g^(-B) S with the causal mask (key > j is zero), as hi/lo bf16 pairs in place.
-            // Key quarter qq (32 keys) is below this warp's rows for qq < dq, holds their
-            // diagonal for qq = dq and lies after them for qq > dq (all zero): warp-uniform.
-            const int dq = 4 * (int)rank + q4;
-            auto convert = [&](const float* x, int qq, uint32_t* pp) {
-                if (qq < dq) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) split2(x[2 * e] * cP, x[2 * e + 1] * cP, pp[e], pp[16 + e]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int kc = 32 * qq + 2 * e;
-                        const float x0 = kc > j ? 0.f : x[2 * e] * cP;
-                        const float x1 = kc + 1 > j ? 0.f : x[2 * e + 1] * cP;
-                        split2(x0, x1, pp[e], pp[16 + e]);
+                    for (int a = 0; a < 2; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf0);
+                    if (c > 0 && !w(&bars.kt_empty1, par(c - 1))) break;
+                    for (int a = 2; a < 4; ++a) tma_load_2d_pair(sk + a * kBox, &mk, 64 * a, r0 + own, kf1);
+                    // V: all keys of the chunk, own 64 value columns (after the previous P.Vz)
+                    if (c > 0 && !w(&bars.v_empty, par(c - 1))) break;
+                    mbar_arrive_expect_tx(&bars.v_full, 2 * kBox);
+                    for (int j = 0; j < 2; ++j) tma_load_2d(sv + j * kBox, &mv, vcol, r0 + 128 * j, &bars.v_full);
+                    ++v_loads;
+                    // K^T operand of the state update: the peer key block x own dk half goes
+                    // into boxes 2*peer, 2*peer+1 once S has read them (the odd CTA's after S's
+                    // first half, the even CTA's after all of S)
+                    if (!w(rank == 1 ? &bars.s_half : &bars.s_full, par(c))) break;
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(&bars.kt_full0, 2 * kBox);
+                        mbar_arrive_expect_tx(&bars.kt_full1, 2 * kBox);
+                        ++armed_kt;
                     }
+                    for (int m = 0; m < 2; ++m)
+                        tma_load_2d_pair(sk + (2 * (int)peer + m) * kBox, &mk, 64 * (2 * (int)rank + m),
+                                         r0 + other, ktf);
+                    // the next chunk's boxes into L2, behind this chunk's loads in the TMA queue
+                    prefetch(c + 1);
                 }
-            };
-            // output rows of chunk c: xi_j * O for this warp's 64 columns, straight from
-            // registers.  Each 128-byte row segment (32 fp32 or 64 bf16 columns = 8 items of
-            // 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so that every
-            // store instruction writes four whole 128-byte segments.  The last TMEM read
-            // releases O for the next Q.R.
-            const float xi = exp2f(l2g * (float)(j + 1));
-            auto do_out = [&](int c) {
-                if (!wait(&bars.o_full, (uint32_t)c & 1u)) return;
-                tc_fence_after();
-                const int p8 = lane & 7;
-                const size_t row0 = (size_t)bh * N + (size_t)c * kB + (size_t)(j - p8);
-                constexpr int kSegs = OUT_BF16 ? 1 : 2;           // 128-byte segments per 64 columns
-                constexpr int kSegCols = OUT_BF16 ? 64 : 32;
-#pragma unroll 1
-                for (int sg = 0; sg < kSegs; ++sg) {
-                    uint32_t a[8][4];
-                    const uint32_t tc0 = tmem + lrow + kTO + 64 * half + kSegCols * sg;
-                    if (OUT_BF16) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            float o[32];
-                            tmem_ld32(tc0 + 32 * hh, o);
-                            tmem_wait_ld();
-                            if (hh == 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                                for (int w = 0; w < 4; ++w)
-                                    a[4 * hh + k][w] =
-                                        pack_bf16(xi * o[8 * k + 2 * w], xi * o[8 * k + 2 * w + 1]);
+                if (!ok) {
+                    // let loads in flight land before the CTAs unwind
+                    const uint32_t b0 = (uint32_t)base;
+                    if (v_loads) mbar_wait(&bars.v_full, (b0 + v_loads - 1) & 1, nullptr, 100000000ull);
+                    if (rank == 0) {
+                        if (armed_q) mbar_wait(&bars.q_full, (b0 + armed_q - 1) & 1, nullptr, 100000000ull);
+                        if (armed_k) {
+                            mbar_wait(&bars.k_full0, (b0 + armed_k - 1) & 1, nullptr, 100000000ull);
+                            mbar_wait(&bars.k_full1, (b0 + armed_k - 1) & 1, nullptr, 100000000ull);
                         }
-                    } else {
-                        float o[32];
-                        tmem_ld32(tc0, o);
-                        tmem_wait_ld();
-                        if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
-                    }
-                    transpose8x8(a, p8);
-                    const size_t col = (size_t)blk * 128 + (size_t)(64 * half + kSegCols * sg);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        uint4* dst;
-                        if (OUT_BF16)
-                            dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
-                                                           (row0 + k) * dv + col) + p8;
-                        else
-                            dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) +
-                                                           (row0 + k) * dv + col) + p8;
-                        *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
+                        if (armed_kt) {
+                            mbar_wait(&bars.kt_full0, (b0 + armed_kt - 1) & 1, nullptr, 100000000ull);
+                            mbar_wait(&bars.kt_full1, (b0 + armed_kt - 1) & 1, nullptr, 100000000ull);
+                        }
                     }
                 }
-            };
-            for (int c = 0; c < nchunks && ok; ++c) {
-                if (!wait(&bars.s_full, (uint32_t)c & 1u)) break;
-                tc_fence_after();
+            }
+        } else if (warp == 1) {
+            // -------------------------------------------------------- MMA issuer (even CTA)
+            if (rank == 0 && lane == 0) {
+                const uint32_t id_s = idesc_bf16(256, 256, 0, 0);     // Q K^T: both K-major
+                const uint32_t id_r = idesc_bf16(256, 128, 1, 1);     // K^T Vz: both MN-major
+                const int fmt = f16 ? 0 : 1;                          // fp16 / bf16 operands
+                const uint32_t id_q = idesc_f16(256, 128, 0, 1, fmt); // Q R': B MN-major
+                const uint32_t id_p = idesc_f16(256, 128, 0, 1, fmt); // P Vz: A in TMEM
+                // descriptors are linear in the start address: base descriptor + offset / 16
+                const uint64_t dQ = sdesc_sw128(smem_u32(sq), 16, 1024);
+                const uint64_t dK = sdesc_sw128(smem_u32(sk), 16, 1024);
+                const uint64_t dKT = sdesc_sw128(smem_u32(sk), kBox, 1024);   // dk boxes 16 KB apart
+                const uint64_t dV = sdesc_sw128(smem_u32(sv), 2 * kBox, 1024);
+                const uint64_t dV16 = sdesc_sw128(smem_u32(sv16), 2 * kBox, 1024);  // hi/lo: R' lo
+                const uint64_t dR16 = sdesc_sw128(smem_u32(sr16), 2 * kBox, 1024);  // hi/lo: R' hi
+                bool ok = !*abort_p;
+                auto w = [&](uint64_t* bar, uint32_t p) {
+                    if (ok && !mbar_wait_cl(bar, p, abort_p)) { ok = false; fail(); }
+                    return ok;
+                };
+                auto s_boxes = [&](int a0) {
 #pragma unroll 1
-                for (int qq = 4 * half; qq < 4 * half + 4; ++qq) {
+                    for (int a = a0; a < a0 + 2; ++a)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t off = (uint64_t)((a * kBox + kk * 32) >> 4);
+                            mma_pair(tmem + kTS, dQ + off, dK + off, id_s, (a | kk) != 0);
+                        }
+                };
+                auto qr_boxes = [&](int a0) {
+#pragma unroll 1
+                    for (int a = a0; a < a0 + 2; ++a)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t qa = dQ + (uint64_t)((a * kBox + kk * 32) >> 4);
+                            const uint64_t ro = (uint64_t)(((4 * a + kk) * 2048) >> 4);
+                            mma_pair(tmem + kTO, qa, dR16 + ro, id_q, (a | kk) != 0);
+                            if (!f16) mma_pair(tmem + kTO, qa, dV16 + ro, id_q, 1);
+                        }
+                };
+                auto kv_block = [&](int j) {
+#pragma unroll
+                    for (int t = 8 * j; t < 8 * j + 8; ++t) {
+                        const uint64_t ka = (uint64_t)(((t >> 3) * 2 * kBox + (t & 7) * 2048) >> 4);
+                        const uint64_t off = (uint64_t)((t * 2048) >> 4);
+                        mma_pair(tmem + kTR, dKT + ka, dV + off, id_r, 1);
+                    }
+                };
+                for (int c = 0; c < nchunks && ok; ++c) {
+                    const uint32_t ph = par(c);
+                    // S = Q K^T (the previous P.Vz, issued earlier, reads the S columns first:
+                    // tcgen05.mma operations of one thread run in issue order)
+                    if (!w(&bars.q_full, ph) || !w(&bars.k_full0, ph)) break;
+                    tc_fence_after();
+                    s_boxes(0);
+                    mma_commit_pair(&bars.s_half, kBoth);
+                    if (!w(&bars.k_full1, ph)) break;
+                    tc_fence_after();
+                    s_boxes(2);
+                    mma_commit_pair(&bars.s_full, kBoth);
+                    // O = Q R'; the first MMA overwrites the accumulator.  fp16: each Q half
+                    // once the conversion warps have turned it into fp16
+                    if (!w(&bars.rcopy, ph)) break;
+                    if (c > 0 && !w(&bars.o_free, par(c - 1))) break;
+                    if (f16 && !w(&bars.q16_0, ph)) break;
+                    tc_fence_after();
+                    qr_boxes(0);
+                    if (f16 && !w(&bars.q16_1, ph)) break;
+                    tc_fence_after();
+                    qr_boxes(2);
+                    mma_commit_pair(&bars.q_empty, kBoth);
+                    // R += K^T Vz (R was rescaled by g^B with the copy), key block 0 then 1
+                    if (!w(&bars.vz_ready, ph) || !w(&bars.kt_full0, ph)) break;
+                    tc_fence_after();
+                    kv_block(0);
+                    mma_commit_pair(&bars.kt_empty0, kBoth);
+                    if (!w(&bars.kt_full1, ph)) break;
+                    tc_fence_after();
+                    kv_block(1);
+                    mma_commit_pair(&bars.kt_empty1, kBoth);
+                    mma_commit_pair(&bars.r_done, kBoth);
+                    // O += P Vz16 (fp16), or (P_hi + P_lo) Vz (bf16 hi/lo)
+                    if (!w(&bars.p_ready, ph)) break;
+                    tc_fence_after();
+                    if (f16) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            mma_pair_ts(tmem + kTO, tmem + kTS + 32 * (t >> 1) + 8 * (t & 1),
+                                        dV16 + (uint64_t)((t * 2048) >> 4), id_p, 1);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const uint32_t a_hi = tmem + kTS + 32 * (t >> 1) + 8 * (t & 1);
+                            const uint64_t bd = dV + (uint64_t)((t * 2048) >> 4);
+                            mma_pair_ts(tmem + kTO, a_hi, bd, id_p, 1);
+                            mma_pair_ts(tmem + kTO, a_hi + 16, bd, id_p, 1);
+                        }
+                    }
+                    mma_commit_pair(&bars.o_full, kBoth);
+                    mma_commit_pair(&bars.v_empty, kBoth);
+                }
+                // every issued MMA completes before the next pass or the release of TMEM
+                mma_commit_pair(&bars.drain, 1);
+                mbar_wait(&bars.drain, drains & 1, nullptr, 200000000ull);
+                ++drains;
+            }
+        } else {
+            // -------------------------------------------------------- transform warps
+            const int q4 = warp & 3;                     // TMEM lane quarter of this warp
+            const int row = 32 * q4 + lane;              // TMEM lane
+            const uint32_t lrow = (uint32_t)(32 * q4) << 16;
+            const int j = 128 * (int)rank + row;         // query row in the chunk / dk row of R
+            const float l2g = dc.l2g[head];
+            bool ok = !*abort_p;
+            // tcgen05.ld/st are warp-collective: keep the outcome of every wait uniform
+            auto wait = [&](uint64_t* bar, uint32_t p) {
+                if (!ok) return false;
+                const bool got = __all_sync(0xffffffffu, mbar_wait(bar, p, abort_p));
+                if (!got) { ok = false; if (lane == 0) fail(); }
+                return ok;
+            };
+            auto arrive_lead = [&](uint64_t* bar) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(lead(bar));
+            };
+            if (warp < kFirstR) {
+                // ---------------------------------------------- scores -> P, then output
+                const int half = (warp - kFirstP) >> 2;  // key half (P) / 64-column half (O)
+                const float sa = dc.a[head];
+                // P = a S with the causal mask (key > j is zero).  Key quarter qq (32 keys)
+                // is below this warp's rows for qq < dq, holds their diagonal for qq = dq and
+                // lies after them for qq > dq (all zero): warp-uniform.
+                const int dq = 4 * (int)rank + q4;
+                float pmax = 0.f;
+                auto scaled = [&](const float* x, int qq, int e) {
+                    const int kc = 32 * qq + e;
+                    return (qq < dq || kc <= j) ? x[e] * sa : 0.f;
+                };
+                const float xi = exp2f(l2g * ((float)(j + 1) - 0.5f * (float)kB));
+                // output rows of chunk c: xi_j * O for this warp's 64 columns, straight from
+                // registers.  Each 128-byte row segment (32 fp32 or 64 bf16 columns = 8 items
+                // of 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so
+                // that every store instruction writes four whole 128-byte segments.  The last
+                // TMEM read releases O for the next Q.R.
+                auto do_out = [&](int c) {
+                    if (!wait(&bars.o_full, par(c))) return;
+                    tc_fence_after();
+                    const int p8 = lane & 7;
+                    const size_t row0 = (size_t)bh * N + (size_t)c * kB + (size_t)(j - p8);
+                    constexpr int kSegs = OUT_BF16 ? 1 : 2;       // 128-byte segments per 64 columns
+                    constexpr int kSegCols = OUT_BF16 ? 64 : 32;
+#pragma unroll 1
+                    for (int sg = 0; sg < kSegs; ++sg) {
+                        uint32_t a[8][4];
+                        const uint32_t tc0 = tmem + lrow + kTO + 64 * half + kSegCols * sg;
+                        if (OUT_BF16) {
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                float o[32];
+                                tmem_ld32(tc0 + 32 * hh, o);
+                                tmem_wait_ld();
+                                if (hh == 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                                    for (int w = 0; w < 4; ++w)
+                                        a[4 * hh + k][w] =
+                                            pack_bf16(xi * o[8 * k + 2 * w], xi * o[8 * k + 2 * w + 1]);
+                            }
+                        } else {
+                            float o[32];
+                            tmem_ld32(tc0, o);
+                            tmem_wait_ld();
+                            if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
+                        }
+                        transpose8x8(a, p8);
+                        const size_t col = (size_t)blk * 128 + (size_t)(64 * half + kSegCols * sg);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            uint4* dst;
+                            if (OUT_BF16)
+                                dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
+                                                               (row0 + k) * dv + col) + p8;
+                            else
+                                dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) +
+                                                               (row0 + k) * dv + col) + p8;
+                            *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
+                        }
+                    }
+                };
+                // one key quarter: fp16 pairs (16 columns) or bf16 hi/lo pairs (32 columns)
+                auto quarter = [&](int qq, auto fmt) {
+                    constexpr bool F16 = decltype(fmt)::value;
                     const uint32_t ts = tmem + lrow + kTS + 32 * qq;
-                    uint32_t pp[32];
+                    uint32_t pp[F16 ? 16 : 32];
                     if (qq <= dq) {
                         float x[32];
                         tmem_ld32(ts, x);
                         tmem_wait_ld();
-                        convert(x, qq, pp);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float y0 = scaled(x, qq, 2 * e), y1 = scaled(x, qq, 2 * e + 1);
+                            if (F16) {
+                                pmax = fmaxf(pmax, fmaxf(fabsf(y0), fabsf(y1)));
+                                pp[e] = pack_f16(y0, y1);
+                            } else {
+                                split2(y0, y1, pp[e], pp[(16 + e) % (F16 ? 16 : 32)]);
+                            }
+                        }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) pp[e] = 0u;
+                        for (int e = 0; e < (F16 ? 16 : 32); ++e) pp[e] = 0u;
                     }
-                    tmem_st32(ts, reinterpret_cast<const float*>(pp));
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                arrive_lead(&bars.p_ready);
-                // while the chunk's P.Vz runs nothing is left to do; then its output
-                do_out(c);
-            }
-        } else {
-            // -------------------------------------------------- state copy, then V -> Vz
-            const int g = warp - kFirstR;            // 0..7
-            const bool remote = g >= 4;              // peer's 64 columns (else this CTA's own)
-            const uint32_t cbase = 64u * (remote ? peer : rank);   // TMEM column of the 64
-            const float gB = dc.gB[head];
-            const uint32_t hi_peer = map_peer(rhi, peer);
-            const uint32_t lo_peer = map_peer(rlo, peer);
-            // State copy for chunk c: the hi/lo bf16 copy of R_{i-1} (this CTA's dk row j,
-            // 64 value columns) into the B operand of Q.R, and R <- g^B R in TMEM, in two
-            // halves of 32 columns (4 items of 16 bytes per row).  Own columns go to this
-            // CTA's copy; the peer's columns are transposed within 4-lane groups so that
-            // each remote store writes 64 contiguous bytes of a row of the peer's copy.
-            // R_{-1} comes from state_in (zero without it).
-            const int p4 = lane & 3;
-            const uint32_t j0 = (uint32_t)(j - p4);
-            auto do_state = [&](int c) {
-                if (c > 0) {
-                    if (!wait(&bars.r_done, (uint32_t)(c - 1) & 1u)) return;
+                    if (F16) tmem_st16(ts, pp);
+                    else tmem_st32(ts, reinterpret_cast<const float*>(pp));
+                };
+                // V row kr of chunk c scaled in place by g^(B-1-kr), one key row per thread;
+                // fp16: also the fp16 copy Vz16.  The block lands after the previous P.Vz.
+                const int kr = 32 * (warp - kFirstP) + lane;
+                const float fz = exp2f(l2g * (float)(kB - 1 - kr));
+                float vmax = 0.f;
+                auto do_v = [&](int c) {
+                    if (!wait(&bars.v_full, par(c))) return;
+                    {
+                        const uint32_t rowoff = (uint32_t)kr * 128u;
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            const uint32_t off = rowoff + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4);
+                            uint4* pv = reinterpret_cast<uint4*>(sv + off);
+                            const uint4 u = *pv;
+                            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+                            uint32_t ob[4], oh[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float y0 = bf16_lo(wv[e]) * fz, y1 = bf16_hi(wv[e]) * fz;
+                                ob[e] = pack_bf16(y0, y1);
+                                if (f16) vmax = fmaxf(vmax, fmaxf(fabsf(y0), fabsf(y1)));
+                                oh[e] = pack_f16(y0, y1);
+                            }
+                            *pv = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                            if (f16) *reinterpret_cast<uint4*>(sv16 + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        }
+                    }
+                    fence_proxy_async();
+                    arrive_lead(&bars.vz_ready);
+                };
+                for (int c = 0; c < nchunks && ok; ++c) {
+                    // V of this chunk (it lands while S runs), then P, then after P.Vz the output
+                    do_v(c);
+                    if (!wait(&bars.s_full, par(c))) break;
                     tc_fence_after();
-                }
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
+                    for (int qq = 4 * half; qq < 4 * half + 4; ++qq) {
+                        if (f16) quarter(qq, std::true_type{});
+                        else quarter(qq, std::false_type{});
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    arrive_lead(&bars.p_ready);
+                    do_out(c);
+                }
+                if (f16) out_of_range(fmaxf(pmax, vmax));
+            } else {
+                // ---------------------------------------------- state copy; Q16 or V -> Vz
+                const int g = warp - kFirstR;            // 0..7
+                const bool remote = g >= 4;              // peer's 64 columns (else this CTA's own)
+                const uint32_t cbase = 64u * (remote ? peer : rank);   // TMEM column of the 64
+                const float gB = dc.gB[head], sc = dc.c[head];
+                // fp16 R'16 (or the bf16 hi part) and, for hi/lo, the lo part
+                const uint32_t hi_peer = map_peer(sr16, peer);
+                const uint32_t lo_peer = map_peer(sv16, peer);
+                const int p4 = lane & 3;
+                const uint32_t j0 = (uint32_t)(j - p4);
+                float cmax = 0.f;
+                // State copy for chunk c: R' = c R_{i-1} (this CTA's dk row j, 64 value
+                // columns) into the B operand of Q.R', and R <- g^B R in TMEM, in two halves
+                // of 32 columns (4 items of 16 bytes per row).  Own columns go to this CTA's
+                // copy; the peer's columns are transposed within 4-lane groups so that each
+                // remote store writes 64 contiguous bytes of a row of the peer's copy.
+                // R_{-1} comes from state_in (zero without it).
+                auto state_half = [&](int c, int hh, auto fmt) {
+                    constexpr bool F16 = decltype(fmt)::value;
                     const uint32_t tcol = tmem + lrow + kTR + cbase + 32 * hh;
                     float x[32];
                     if (c == 0) {
@@ -512,7 +614,14 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     for (int k = 0; k < 4; ++k)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            split2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1], h[k][e], l[k][e]);
+                            const float y0 = sc * x[8 * k + 2 * e], y1 = sc * x[8 * k + 2 * e + 1];
+                            if (F16) {
+                                cmax = fmaxf(cmax, fmaxf(fabsf(y0), fabsf(y1)));
+                                h[k][e] = pack_f16(y0, y1);
+                                l[k][e] = 0u;
+                            } else {
+                                split2(y0, y1, h[k][e], l[k][e]);
+                            }
                             x[8 * k + 2 * e] *= gB;
                             x[8 * k + 2 * e + 1] *= gB;
                         }
@@ -521,75 +630,107 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     if (remote) {
                         // lane p of a 4-lane group then holds item 4hh+p of row j0 + k in slot k
                         transpose4x4(h, p4);
-                        transpose4x4(l, p4);
+                        if (!F16) transpose4x4(l, p4);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint32_t r = j0 + (uint32_t)k;
                             const uint32_t off =
                                 r * 128u + ((((uint32_t)(4 * hh + p4)) ^ (r & 7u)) << 4);
                             st_cluster_v4(hi_peer + off, h[k][0], h[k][1], h[k][2], h[k][3]);
-                            st_cluster_v4(lo_peer + off, l[k][0], l[k][1], l[k][2], l[k][3]);
+                            if (!F16) st_cluster_v4(lo_peer + off, l[k][0], l[k][1], l[k][2], l[k][3]);
                         }
                     } else {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint32_t off = (uint32_t)j * 128u +
                                                  ((((uint32_t)(4 * hh + k)) ^ ((uint32_t)j & 7u)) << 4);
-                            *reinterpret_cast<uint4*>(rhi + off) = make_uint4(h[k][0], h[k][1], h[k][2], h[k][3]);
-                            *reinterpret_cast<uint4*>(rlo + off) = make_uint4(l[k][0], l[k][1], l[k][2], l[k][3]);
+                            *reinterpret_cast<uint4*>(sr16 + off) = make_uint4(h[k][0], h[k][1], h[k][2], h[k][3]);
+                            if (!F16)
+                                *reinterpret_cast<uint4*>(sv16 + off) =
+                                    make_uint4(l[k][0], l[k][1], l[k][2], l[k][3]);
                         }
                     }
-                }
-                tmem_wait_st();
-                if (remote) fence_proxy_async_cluster(); else fence_proxy_async();
-                tc_fence_before();
-                arrive_lead(&bars.rcopy);
-            };
-            // V row kr of chunk c scaled in place by g^(B-1-kr); the block lands after the
-            // previous P.Vz, while this group copies the state
-            const int kr = 32 * g + lane;
-            const float fz = exp2f(l2g * (float)(kB - 1 - kr));
-            auto do_v = [&](int c) {
-                if (!wait(&bars.v_full, (uint32_t)c & 1u)) return;
-                uint8_t* vrow = sv + kr * 128;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint4* pv = reinterpret_cast<uint4*>(vrow + (((uint32_t)cc ^ ((uint32_t)kr & 7u)) << 4));
-                    uint4 u = *pv;
-                    uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) wv[e] = pack_bf16(bf16_lo(wv[e]) * fz, bf16_hi(wv[e]) * fz);
-                    *pv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
-                fence_proxy_async();
-                arrive_lead(&bars.vz_ready);
-            };
-            for (int c = 0; c < nchunks && ok; ++c) {
-                do_state(c);
-                do_v(c);
-            }
-            // ---- final state: this CTA's dk rows of R_{N/B-1}, this warp's 64 columns
-            if (ok && state_out && nchunks > 0) {
-                if (wait(&bars.r_done, (uint32_t)(nchunks - 1) & 1u)) {
-                    tc_fence_after();
+                };
+                auto do_state = [&](int c) {
+                    if (c > 0) {
+                        if (!wait(&bars.r_done, par(c - 1))) return;
+                        tc_fence_after();
+                    }
 #pragma unroll 1
                     for (int hh = 0; hh < 2; ++hh) {
-                        float x[32];
-                        tmem_ld32(tmem + lrow + kTR + cbase + 32 * hh, x);
-                        tmem_wait_ld();
-                        float4* dst = reinterpret_cast<float4*>(
-                            state_out + ((size_t)bh * kDk + j) * dv + blk * 128 + cbase + 32 * hh);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+                        if (f16) state_half(c, hh, std::true_type{});
+                        else state_half(c, hh, std::false_type{});
                     }
+                    tmem_wait_st();
+                    if (remote) fence_proxy_async_cluster(); else fence_proxy_async();
+                    tc_fence_before();
+                    arrive_lead(&bars.rcopy);
+                };
+                // Q -> fp16 in place, one row of one dk box per thread: boxes 2h, 2h+1 once S
+                // has read them (warps 10-13 the first, 14-17 the second)
+                const int qrow = 32 * (g & 3) + lane;
+                auto do_q16 = [&](int c, int hq) {
+                    if (!wait(hq == 0 ? &bars.s_half : &bars.s_full, par(c))) return;
+                    {
+                        const int a = 2 * hq + (g >> 2);
+                        uint8_t* qr = sq + a * kBox + qrow * 128;
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            // visit the row's items in swizzled order: the 8 rows of an 8-lane
+                            // group then touch 8 different bank groups (conflict-free)
+                            uint4* p = reinterpret_cast<uint4*>(qr + (((uint32_t)cc ^ ((uint32_t)qrow & 7u)) << 4));
+                            const uint4 u = *p;
+                            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float y0 = bf16_lo(wv[e]), y1 = bf16_hi(wv[e]);
+                                cmax = fmaxf(cmax, fmaxf(fabsf(y0), fabsf(y1)));
+                                o[e] = pack_f16(y0, y1);
+                            }
+                            *p = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                    fence_proxy_async();
+                    arrive_lead(hq == 0 ? &bars.q16_0 : &bars.q16_1);
+                };
+                for (int c = 0; c < nchunks && ok; ++c) {
+                    do_state(c);
+                    if (f16) { do_q16(c, 0); do_q16(c, 1); }
                 }
+                if (f16) out_of_range(cmax);
             }
         }
+        // ---------------------------------------------------------- end of the pass
+        __syncwarp();
+        tc_fence_before();
+        cluster_sync_all();     // every MMA of the pass has completed (drain), both CTAs' flags set
+        tc_fence_after();
+        if (pass == 1 || !f16 || *abort_p || !*range_p) break;
+        if (threadIdx.x == 0 && rank == 0) atomicAdd(&g_reruns_chunkwise_pair, 1u);
     }
-    __syncwarp();
+    // ---- final state: this CTA's dk rows of R_{N/B-1}, each state-copy warp its 64 columns
+    // (written after the last pass, so that a re-run still reads an aliased state_in intact;
+    // both formats give the same state: its update reads bf16 operands only)
+    if (warp >= kFirstR && state_out && nchunks > 0 && !*abort_p) {
+        const int q4 = warp & 3;
+        const uint32_t lrow = (uint32_t)(32 * q4) << 16;
+        const int j = 128 * (int)rank + 32 * q4 + lane;
+        const uint32_t cbase = 64u * ((warp - kFirstR >= 4) ? peer : rank);
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[32];
+            tmem_ld32(tmem + lrow + kTR + cbase + 32 * hh, x);
+            tmem_wait_ld();
+            float4* dst = reinterpret_cast<float4*>(
+                state_out + ((size_t)bh * kDk + j) * dv + blk * 128 + cbase + 32 * hh);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+        }
+    }
     tc_fence_before();
-    cluster_sync_all();     // no MMA in flight, no remote access pending
+    cluster_sync_all();     // no tensor-memory access pending in either CTA
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem, 512);
@@ -611,10 +752,14 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
                                      cudaStream_t s) {
     if (!chunkwise_pair_supported(dk, dv, chunk, hc, H)) return cudaErrorNotSupported;
     Decay dc;
+    int fp16_first = 1;
     for (int h = 0; h < H; ++h) {
         dc.l2g[h] = hc.l2g[h];
         dc.gB[h] = hc.gB[h];
-        dc.cP[h] = hc.ginvB[h];
+        dc.a[h] = exp2f(-0.5f * (float)chunk * hc.l2g[h]);
+        dc.c[h] = exp2f(0.5f * (float)chunk * hc.l2g[h]);
+        // fp16 Vz keeps ~11 bits down to g^(B-1) |v| only while g^(-B) <= 4096
+        if (!(hc.l2g[h] * (float)chunk >= -12.0f)) fp16_first = 0;
     }
     const long long rows = (long long)b * H * N;
     if (rows >= (1LL << 31)) return cudaErrorNotSupported;
@@ -628,7 +773,8 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     auto kern = out_bf16 ? chunkwise_pair_kernel<true> : chunkwise_pair_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv, dc);
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv,
+                                                fp16_first, dc);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
     return e;
@@ -640,6 +786,16 @@ unsigned read_clear_error_tc_chunkwise_pair(cudaStream_t s) {
                                   s) != cudaSuccess)
         return 0;
     cudaMemcpyToSymbolAsync(g_err_chunkwise_pair, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s);
+    cudaStreamSynchronize(s);
+    return h;
+}
+
+unsigned read_clear_reruns_tc_chunkwise_pair(cudaStream_t s) {
+    unsigned h = 0, z = 0;
+    if (cudaMemcpyFromSymbolAsync(&h, g_reruns_chunkwise_pair, sizeof(h), 0,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return 0;
+    cudaMemcpyToSymbolAsync(g_reruns_chunkwise_pair, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s);
     cudaStreamSynchronize(s);
     return h;
 }

@@ -154,3 +154,58 @@ def test_tc_chunkwise_pair_edges(b, H, N, dv):
     assert err_bf16(got, want) < TOL_BF16
     assert err_f32(st, s_end) < TOL_BF16
     rb.check_device_error()
+
+
+def test_pair_fp16_format_no_rerun_at_unit_scale_inputs():
+    """The pair kernel's fp16 operands hold N(0,1)/16 inputs without re-running any unit."""
+    b, H, N, dk, dv = 1, 4, 1024, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 400)
+    g = inputs.gammas(H)
+    rb.chunkwise_format_reruns()
+    got = rb.retention_chunkwise(q, k, v, g, 256)
+    assert rb.last_kernel() == "chunkwise_tc_pair"
+    assert rb.chunkwise_format_reruns() == 0
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, 256)) < TOL_BF16
+    rb.check_device_error()
+
+
+@pytest.mark.parametrize("what", ["q_beyond_fp16", "scores_beyond_fp16", "v_beyond_fp16"])
+def test_pair_reruns_units_that_leave_fp16_range(what):
+    """A head whose Q (|q| > 65504), scores (|a q.k| > 65504) or V (|v| > 65504) leave fp16's
+    range re-runs its units in the bf16 hi/lo format inside the same launch: the result
+    still matches the oracle, only that head's dv/128 units re-run, and an aliased incoming
+    state (state_in == state_out) is still read intact by the re-run."""
+    b, H, N, dk, dv = 1, 3, 768, 256, 256
+    q, k, v = mk(b, H, N, dk, dv, 410)
+    if what == "q_beyond_fp16":
+        q[:, 1] *= 2.0 ** 21          # |q| up to ~5e5
+    elif what == "scores_beyond_fp16":
+        q[:, 1] *= 2.0 ** 8
+        k[:, 1] *= 2.0 ** 8           # |q.k| up to ~1e5, times a = g^(-128)
+    else:
+        v[:, 1] *= 2.0 ** 21
+    g = inputs.gammas(H)
+    s0 = inputs.randn((b, H, dk, dv), 415, 0.05, "f32", DEV)
+    st = s0.clone()
+    rb.chunkwise_format_reruns()
+    got = rb.retention_chunkwise(q, k, v, g, 256, state_in=st, state_out=st)
+    assert rb.last_kernel() == "chunkwise_tc_pair"
+    assert rb.chunkwise_format_reruns() == b * (dv // 128)
+    want, want_state = oracle.chunkwise(q, k, v, g, 256, state_in=s0, return_state=True)
+    for h in range(H):
+        assert err_bf16(got[:, h], want[:, h]) < TOL_BF16, h
+        assert err_bf16(st[:, h], want_state[:, h]) < TOL_BF16, h
+    rb.check_device_error()
+
+
+def test_pair_hilo_format_from_the_start_for_small_decays():
+    """Decays with g^(-256) > 4096 take the bf16 hi/lo format from the first pass."""
+    b, H, N, dk, dv = 1, 2, 768, 256, 128
+    q, k, v = mk(b, H, N, dk, dv, 420)
+    g = [0.96, 0.999]
+    rb.chunkwise_format_reruns()
+    got = rb.retention_chunkwise(q, k, v, g, 256)
+    assert rb.last_kernel() == "chunkwise_tc_pair"
+    assert rb.chunkwise_format_reruns() == 0
+    assert err_bf16(got, oracle.chunkwise(q, k, v, g, 256)) < TOL_BF16
+    rb.check_device_error()
