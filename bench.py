@@ -454,6 +454,61 @@ def bench_xpos(args, dist, rb, pk):
                          "algorithmic_bytes_per_launch": nbytes}}
 
 
+def bench_chunkwise_bf16(args, dist, rb, pk):
+    """The headline workload with a bf16 output (the state stays fp32)."""
+    w = inputs.CHUNKWISE_LONG
+    q, k, v = inputs.qkv(w, "cuda")
+    o = torch.empty(w.b, w.H, w.N, w.dv, dtype=torch.bfloat16, device="cuda")
+    fn = lambda: rb.retention_chunkwise(q, k, v, w.gamma, w.chunk, out=o)  # noqa: E731
+    steps = max(3, args.steps // 2)
+    ms, _ = timed(fn, steps, 3, dist)
+    rb.check_device_error()
+    kern = rb.last_kernel()
+    ms_step = ms / steps
+    value, _ = aggregate(dist, ms, w.b * w.N * steps)
+    flops = inputs.algorithmic_flops("chunkwise", w)
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    nbytes = 2 * (2 * w.b * w.H * w.N * w.dk + w.b * w.H * w.N * w.dv) + 2 * w.b * w.H * w.N * w.dv
+    del q, k, v, o
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name} with bf16 output: b{w.b} H{w.H} N{w.N} dk{w.dk} dv{w.dv} chunk "
+                        f"{w.chunk}, bf16 q/k/v, fp32 state, bf16 out ({kern})",
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "achieved_gbs": nbytes / (ms_step * 1e-3) / 1e9}}
+
+
+def bench_sweep(args, dist, rb, pk):
+    """The chunkwise training-shape sweep: b4 H16 dk256 dv512, N x chunk grid, fp32 out."""
+    points = []
+    for w in inputs.SWEEP:
+        q, k, v = inputs.qkv(w, "cuda")
+        o = torch.empty(w.b, w.H, w.N, w.dv, dtype=torch.float32, device="cuda")
+        fn = lambda: rb.retention_chunkwise(q, k, v, w.gamma, w.chunk, out=o)  # noqa: E731
+        steps = max(3, args.steps // 5)
+        ms, _ = timed(fn, steps, 3, dist)
+        rb.check_device_error()
+        kern = rb.last_kernel()
+        ms_step = ms / steps
+        value, _ = aggregate(dist, ms, w.b * w.N * steps)
+        flops = inputs.algorithmic_flops("chunkwise", w)
+        achieved = flops / (ms_step * 1e-3) / 1e12
+        points.append({"N": w.N, "chunk": w.chunk, "kernel": kern, "value": value,
+                       "unit": "tokens/s", "ms_per_step": ms_step,
+                       "roofline": {"bound": "tensor", "achieved": achieved,
+                                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                    "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                                    "algorithmic_flops_per_launch": flops}})
+        del q, k, v, o
+        torch.cuda.empty_cache()
+    return {"workload": "sweep: chunkwise retention b4 H16 dk256 dv512, N in {2048, 8192, 16384} "
+                        "x chunk in {64, 128, 256}, bf16 q/k/v N(0,1)/16, fp32 state and out",
+            "points": points}
+
+
 def cpu_baseline_leg():
     w = inputs.CHUNKWISE_LONG
     threads = max(1, min(os.cpu_count() or 1, w.H))
@@ -464,7 +519,8 @@ def cpu_baseline_leg():
 
 # the legs reported beside the headline, in this order
 EXTRA_LEGS = {"decode": bench_decode, "parallel": bench_parallel, "backward": bench_backward,
-              "rglru": bench_rglru, "xpos": bench_xpos}
+              "rglru": bench_rglru, "xpos": bench_xpos, "chunkwise_bf16": bench_chunkwise_bf16,
+              "sweep": bench_sweep}
 
 
 def run_ours(args, dist: Dist):

@@ -300,6 +300,19 @@ int retention_check_device_error(void* stream);
 int retention_chunkwise_format_reruns(void* stream);
 
 /*
+ * Self-test of the bounded on-chip waits (the pages describe no fault handling; this is the
+ * library's own).  Launches the pair-of-SMs chunkwise kernel on b1 H1 N256 dk256 dv128
+ * (q, k: 256 x 256 bf16, v: 256 x 128 bf16, o: 256 x 128 fp32, DEVICE buffers that are
+ * neither read nor written) with every wait limited to 1 ms and a TMA producer that issues
+ * no load: each wait expires, the kernel unwinds with no copy or MMA in flight, frees its
+ * tensor memory and sets the device error word, so that the next
+ * retention_check_device_error() returns RET_ERR_TIMEOUT.  The device stays usable.
+ * Asynchronous on `stream`; returns RET_ERR_NULL / RET_ERR_ALIGN for bad pointers.
+ */
+int retention_chunkwise_wait_selftest(const void* q, const void* k, const void* v, void* o,
+                                      void* stream);
+
+/*
  * Number of kernels this library has launched in this process so far (all
  * devices, all calls).  Host-side counter, incremented after each successful
  * launch; lets callers count launches inside a timed region.

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.retention_status_string.argtypes = [i]
             L.retention_status_string.restype = ctypes.c_char_p
             L.retention_check_device_error.argtypes = [vp]
+            L.retention_chunkwise_wait_selftest.argtypes = [vp, vp, vp, vp, vp]
+            L.retention_chunkwise_wait_selftest.restype = ctypes.c_int
             L.retention_chunkwise_format_reruns.argtypes = [vp]
             L.retention_chunkwise_format_reruns.restype = ctypes.c_int
             L.retention_kernel_launches.argtypes = []
@@ -383,6 +385,14 @@ def kernel_launches() -> int:
 def last_kernel() -> str:
     """Name of the kernel this host thread launched last (see RET_KERNEL_* codes)."""
     return KERNEL_NAMES.get(int(lib().retention_last_kernel()), "unknown")
+
+
+def chunkwise_wait_selftest(q, k, v, o, stream=None) -> int:
+    """Launch the bounded-wait self-test (q, k: bf16 [256,256], v: bf16 [256,128], o: fp32
+    [256,128] on the device); returns the launch status, the expiry shows up in
+    check_device_error()."""
+    return int(lib().retention_chunkwise_wait_selftest(_ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                       _stream(stream)))
 
 
 def chunkwise_format_reruns(stream=None) -> int:

@@ -100,10 +100,12 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
                                 const HeadConsts& hc, const float* state_in, float* state_out,
                                 cudaStream_t s);
 // Pair-of-SMs chunkwise kernel (cta_group::2): chunk 256, dk 256, dv a multiple of 128.
+// wait_ns bounds every on-chip wait (0: the default of 2 s); no_loads makes the TMA
+// producer issue nothing (self-test of the bounded waits: every wait then expires).
 cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,
-                                     cudaStream_t s);
+                                     cudaStream_t s, uint64_t wait_ns = 0, int no_loads = 0);
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
                                int out_bf16, int b, int H, int N, int dk, int dv,
                                const HeadConsts& hc, unsigned flags, cudaStream_t s);

@@ -312,6 +312,23 @@ const char* retention_cuda_error_string(int cuda_error) {
     return buf;
 }
 
+int retention_chunkwise_wait_selftest(const void* q, const void* k, const void* v, void* o,
+                                      void* stream) {
+    if (!q || !k || !v || !o) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RET_ERR_ALIGN;
+    const int H = 1, N = 256, dk = 256, dv = 128, chunk = 256;
+    const double gamma[1] = {0.96875};
+    HeadConsts hc;
+    int rc = head_consts(gamma, H, chunk, &hc);
+    if (rc != RET_OK) return rc;
+    // every wait gives up after 1 ms; the TMA producer issues no load, so nothing is in
+    // flight when the CTAs unwind
+    return cuda_status(ret::launch_chunkwise_tc_pair(q, k, v, o, 0, 1, H, N, dk, dv, chunk, hc,
+                                                     nullptr, nullptr,
+                                                     static_cast<cudaStream_t>(stream),
+                                                     1000000ull, 1));
+}
+
 int retention_chunkwise_format_reruns(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return -1;

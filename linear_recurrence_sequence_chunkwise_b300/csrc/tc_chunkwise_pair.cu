@@ -154,7 +154,8 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                       const __grid_constant__ CUtensorMap mv,
                       void* __restrict__ out_base, const float* __restrict__ state_in,
                       float* __restrict__ state_out, int N,
-                      int H, int dv, int fp16_first, const Decay dc) {
+                      int H, int dv, int fp16_first, const Decay dc, uint64_t wait_ns,
+                      int no_loads) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = sm + kQOff;
@@ -235,7 +236,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 uint32_t armed_q = 0, armed_k = 0, armed_kt = 0, v_loads = 0;
                 bool ok = !*abort_p;
                 auto w = [&](uint64_t* bar, uint32_t p) {
-                    if (ok && !mbar_wait(bar, p, abort_p)) { ok = false; fail(); }
+                    if (ok && !mbar_wait(bar, p, abort_p, wait_ns)) { ok = false; fail(); }
                     return ok;
                 };
                 // the pairs of one head share Q and K: pull the next chunk's boxes into L2
@@ -249,6 +250,8 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     for (int m = 0; m < 2; ++m) tma_prefetch_l2(&mk, 64 * (2 * (int)rank + m), r0 + other);
                     for (int j = 0; j < 2; ++j) tma_prefetch_l2(&mv, vcol, r0 + 128 * j);
                 };
+                // (self-test of the bounded waits: no load is issued, every wait expires)
+                if (no_loads) ok = false;
                 if (ok) prefetch(0);
                 for (int c = 0; c < nchunks && ok; ++c) {
                     const int r0 = rowbase + c * kB;
@@ -321,7 +324,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 const uint64_t dR16 = sdesc_sw128(smem_u32(sr16), 2 * kBox, 1024);  // hi/lo: R' hi
                 bool ok = !*abort_p;
                 auto w = [&](uint64_t* bar, uint32_t p) {
-                    if (ok && !mbar_wait_cl(bar, p, abort_p)) { ok = false; fail(); }
+                    if (ok && !mbar_wait_cl(bar, p, abort_p, wait_ns)) { ok = false; fail(); }
                     return ok;
                 };
                 auto s_boxes = [&](int a0) {
@@ -421,7 +424,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             // tcgen05.ld/st are warp-collective: keep the outcome of every wait uniform
             auto wait = [&](uint64_t* bar, uint32_t p) {
                 if (!ok) return false;
-                const bool got = __all_sync(0xffffffffu, mbar_wait(bar, p, abort_p));
+                const bool got = __all_sync(0xffffffffu, mbar_wait(bar, p, abort_p, wait_ns));
                 if (!got) { ok = false; if (lane == 0) fail(); }
                 return ok;
             };
@@ -739,6 +742,9 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
 
 }  // namespace
 
+// Every wait of the kernel gives up after this long (wall time) and reports RET_ERR_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 bool chunkwise_pair_supported(int dk, int dv, int chunk, const HeadConsts& hc, int H) {
     if (dk != kDk || chunk != kB || dv % 128 != 0) return false;
     for (int h = 0; h < H; ++h)
@@ -749,8 +755,9 @@ bool chunkwise_pair_supported(int dk, int dv, int chunk, const HeadConsts& hc, i
 cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, uint64_t wait_ns, int no_loads) {
     if (!chunkwise_pair_supported(dk, dv, chunk, hc, H)) return cudaErrorNotSupported;
+    if (wait_ns == 0) wait_ns = kWaitLimitNs;
     Decay dc;
     int fp16_first = 1;
     for (int h = 0; h < H; ++h) {
@@ -774,7 +781,7 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv,
-                                                fp16_first, dc);
+                                                fp16_first, dc, wait_ns, no_loads);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
     return e;

@@ -39,7 +39,8 @@ def test_exports_every_declared_function(L):
                           "retention_chunkwise_host_noalloc",
                           "retention_chunkwise_host_static_scratch_bytes",
                           "retention_chunkwise_backward", "rglru_scan",
-                          "retention_xpos_rotate", "retention_chunkwise_format_reruns"}
+                          "retention_xpos_rotate", "retention_chunkwise_format_reruns",
+                          "retention_chunkwise_wait_selftest"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
