@@ -295,6 +295,54 @@ const char* retention_status_string(int status);
 int retention_check_device_error(void* stream);
 
 /*
+ * The gated multi-scale retention layer, [RN2] "門控多尺度 Retention" (its formula was lost
+ * in extraction; the prose names every step): per head h,
+ *   Q_h = xPos(X W_Q[:, h*dk..]), K_h = xPos(X W_K[:, h*dk..]), V_h = X W_V[:, h*dv..],
+ *   Y_h = retention(Q_h, K_h, V_h, gamma_h)   (parallel form with `flags`, or the
+ *                                             chunkwise form with chunk > 0, unnormalised)
+ *   out = (swish(X W_G) (.) GroupNorm_h(Y)) W_O            (eps as in msr_epilogue)
+ * xPos ([RN2] "Retention" eqs.(2)-(3)) as in retention_xpos_rotate, at positions
+ * pos0 + n; theta NULL means no rotation.
+ * x: [b][N][d_model] bf16; wq, wk: [d_model][H*dk]; wv, wg: [d_model][H*dv];
+ * wo: [H*dv][d_out], all bf16 row-major DEVICE arrays (x W as the layer applies them);
+ * out: [b][N][d_out] in out_dtype; gamma: HOST, H doubles in [0, 1]; theta: HOST, dk/2
+ * doubles or NULL.  workspace: DEVICE memory of retention_msr_layer_workspace_bytes(...)
+ * bytes, 256-byte aligned, owned by the caller (Q, K, V, G and the gated rows live there,
+ * bf16).  Supported: dk in {128, 256}, dv a multiple of 128 (<= 512), d_model a multiple
+ * of 64, H*dk, H*dv and d_out multiples of 256, N >= 128 for the parallel form
+ * (RET_ERR_UNSUPPORTED otherwise); flags must be 0 with chunk > 0.  Asynchronous on
+ * `stream`: six kernels (four projections, retention with the gated epilogue fused --
+ * chunkwise: retention then msr_epilogue --, the output projection).
+ */
+int retention_msr_layer(const void* x, const void* wq, const void* wk, const void* wv,
+                        const void* wg, const void* wo, void* out, ret_dtype out_dtype, int b,
+                        int N, int d_model, int H, int dk, int dv, int d_out,
+                        const double* gamma, const double* theta, long long pos0,
+                        unsigned flags, float eps, int chunk, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of retention_msr_layer (0 for negative sizes).  Host-side. */
+size_t retention_msr_layer_workspace_bytes(int b, int N, int H, int dk, int dv, int chunk);
+
+/*
+ * One projection of the layer: C = A W, A: [M][K] bf16, W: [K][Nc] bf16 (row-major DEVICE
+ * arrays), C: [M][Nc] in c_dtype, fp32 accumulation (tensor cores).  Nc % 256 == 0 and
+ * K % 64 == 0 (RET_ERR_UNSUPPORTED otherwise); any M.
+ */
+int retention_gemm(const void* a, const void* w, void* c, ret_dtype c_dtype, int M, int Nc, int K,
+                   void* stream);
+
+/*
+ * The per-head projection of the layer: out[b][h][n][:] = (x[b][n][:] W)[h*d .. h*d+d-1],
+ * head-major bf16 rows as the retention calls read them, rotated by xPos at position
+ * pos0 + n when theta (HOST, d/2 doubles) is not NULL -- the rotation of
+ * retention_xpos_rotate, fused into the projection.  x: [b][N][d_in] bf16, W: [d_in][H*d]
+ * bf16 (DEVICE).  d a multiple of 64 (<= 256), H*d a multiple of 256, d_in of 64.
+ */
+int retention_project_heads(const void* x, const void* w, void* out, int b, int N, int d_in, int H,
+                            int d, const double* theta, long long pos0, void* stream);
+
+/*
  * Diagnostics of the tensor-core chunkwise kernel for chunk 256, dk 256 (pairs of SMs):
  * it computes the score x value and query x state products with fp16 operands and, if a
  * value it rounds to fp16 lies outside fp16's range (|x| >= 65504), re-runs that unit
@@ -348,7 +396,8 @@ enum {
     RET_KERNEL_CHUNKWISE_TC_PAIR = 8, /* chunkwise form, tensor cores on pairs of SMs */
     RET_KERNEL_CHUNKWISE_BACKWARD_SIMT = 9, /* chunkwise gradient, CUDA-core fp32 FMA   */
     RET_KERNEL_RGLRU = 10,          /* RG-LRU scan                                    */
-    RET_KERNEL_XPOS = 11            /* xPos rotation of Q and K                       */
+    RET_KERNEL_XPOS = 11,           /* xPos rotation of Q and K                       */
+    RET_KERNEL_GEMM_TC = 12         /* projection GEMM of the layer, tensor cores     */
 };
 
 /*

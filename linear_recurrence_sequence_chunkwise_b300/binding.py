@@ -25,7 +25,7 @@ NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
                 5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair",
-                9: "chunkwise_backward_simt", 10: "rglru", 11: "xpos"}
+                9: "chunkwise_backward_simt", 10: "rglru", 11: "xpos", 12: "gemm_tc"}
 
 _lib = None
 _lock = threading.Lock()
@@ -79,6 +79,17 @@ def lib() -> ctypes.CDLL:
             L.retention_status_string.argtypes = [i]
             L.retention_status_string.restype = ctypes.c_char_p
             L.retention_check_device_error.argtypes = [vp]
+            L.retention_msr_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i,
+                                              dp, dp, ctypes.c_longlong, u, f, i, vp,
+                                              ctypes.c_size_t, vp]
+            L.retention_msr_layer.restype = ctypes.c_int
+            L.retention_msr_layer_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            L.retention_msr_layer_workspace_bytes.restype = ctypes.c_size_t
+            L.retention_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            L.retention_gemm.restype = ctypes.c_int
+            L.retention_project_heads.argtypes = [vp, vp, vp, i, i, i, i, i, dp, ctypes.c_longlong,
+                                                  vp]
+            L.retention_project_heads.restype = ctypes.c_int
             L.retention_chunkwise_wait_selftest.argtypes = [vp, vp, vp, vp, vp]
             L.retention_chunkwise_wait_selftest.restype = ctypes.c_int
             L.retention_chunkwise_format_reruns.argtypes = [vp]
@@ -385,6 +396,76 @@ def kernel_launches() -> int:
 def last_kernel() -> str:
     """Name of the kernel this host thread launched last (see RET_KERNEL_* codes)."""
     return KERNEL_NAMES.get(int(lib().retention_last_kernel()), "unknown")
+
+
+def _doubles(vals):
+    if vals is None:
+        return None
+    v = [float(x) for x in vals]
+    return (ctypes.c_double * max(len(v), 1))(*v)
+
+
+def retention_gemm(a, w, out=None, out_dtype=torch.float32, stream=None):
+    """C = A W (tensor cores): a [M, K] bf16, w [K, Nc] bf16 -> [M, Nc]."""
+    M, K = a.shape
+    Nc = w.shape[1]
+    if a.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("a and w are bf16")
+    if out is None:
+        out = torch.empty((M, Nc), dtype=out_dtype, device=a.device)
+    rc = lib().retention_gemm(_ptr(a), _ptr(w), _ptr(out), _dtype_code(out.dtype), M, Nc, K,
+                              _stream(stream))
+    _check("retention_gemm", rc)
+    return out
+
+
+def retention_project_heads(x, w, H: int, d: int, theta=None, pos0: int = 0, out=None,
+                            stream=None):
+    """Head-major projection with the xPos rotation fused: x [b, N, d_in] bf16, w [d_in, H*d]
+    bf16 -> [b, H, N, d] bf16."""
+    b, N, d_in = x.shape
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("x and w are bf16")
+    if theta is not None and len(theta) != d // 2:
+        raise ValueError("theta needs d/2 angles")
+    if out is None:
+        out = torch.empty((b, H, N, d), dtype=torch.bfloat16, device=x.device)
+    rc = lib().retention_project_heads(_ptr(x), _ptr(w), _ptr(out), b, N, d_in, H, d,
+                                       _doubles(theta), int(pos0), _stream(stream))
+    _check("retention_project_heads", rc)
+    return out
+
+
+def msr_layer_workspace_bytes(b: int, N: int, H: int, dk: int, dv: int, chunk: int = 0) -> int:
+    return int(lib().retention_msr_layer_workspace_bytes(b, N, H, dk, dv, chunk))
+
+
+def retention_msr_layer(x, wq, wk, wv, wg, wo, gamma, theta=None, pos0: int = 0, flags: int = 0,
+                        eps: float = 1e-5, chunk: int = 0, out=None, out_dtype=torch.float32,
+                        workspace=None, stream=None):
+    """Gated multi-scale retention layer: x [b, N, D] bf16; wq, wk [D, H*dk]; wv, wg [D, H*dv];
+    wo [H*dv, Dout] (bf16).  Returns [b, N, Dout]."""
+    b, N, D = x.shape
+    H = len(gamma)
+    dk, dv, Dout = wq.shape[1] // H, wv.shape[1] // H, wo.shape[1]
+    for t in (x, wq, wk, wv, wg, wo):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("x and the weights are bf16")
+    if out is None:
+        out = torch.empty((b, N, Dout), dtype=out_dtype, device=x.device)
+    owned = workspace is None
+    if owned:
+        nbytes = msr_layer_workspace_bytes(b, N, H, dk, dv, chunk)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    rc = lib().retention_msr_layer(_ptr(x), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wg), _ptr(wo),
+                                   _ptr(out), _dtype_code(out.dtype), b, N, D, H, dk, dv, Dout,
+                                   _gamma(gamma, H), _doubles(theta), int(pos0), flags,
+                                   float(eps), chunk, ctypes.c_void_p(workspace.data_ptr()),
+                                   ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if owned:
+        workspace.record_stream(stream or torch.cuda.current_stream(x.device))
+    _check("retention_msr_layer", rc)
+    return out
 
 
 def chunkwise_wait_selftest(q, k, v, o, stream=None) -> int:
