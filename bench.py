@@ -295,14 +295,50 @@ def bench_chunkwise(args, dist, rb, pk, out_dtype):
     ms_e2e, _ = timed(e2e_step, e2e_steps, 1, dist)
     e2e_val, _ = aggregate(dist, ms_e2e, tokens * e2e_steps)
     rb.check_device_error()
+    link = host_link(((hq, q), (hk, k), (hv, v)), ((o, ho),))
+    e2e_ms = ms_e2e / e2e_steps
     res["e2e"] = {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": in_bytes,
-                  "d2h_bytes_per_step": out_bytes, "ms_per_step": ms_e2e / e2e_steps,
+                  "d2h_bytes_per_step": out_bytes, "ms_per_step": e2e_ms,
                   "mode": f"retention_chunkwise_host: pinned host q/k/v/out, {w.N // seg} segments "
                           f"of {seg} tokens, H2D / compute / D2H on three streams, state carried "
-                          f"on the device"}
+                          f"on the device",
+                  "link": link,
+                  "link_frac": link["both_ms"] / e2e_ms}
     del q, k, v, o, hq, hk, hv, ho
     torch.cuda.empty_cache()
     return res
+
+
+def host_link(h2d_pairs, d2h_pairs, reps: int = 3) -> dict:
+    """The host link measured with the step's own pinned buffers: the H2D copies alone,
+    the D2H copies alone and both at once on two streams (copy engines only, no kernel).
+    both_ms is the floor of an end-to-end step that moves these bytes."""
+    sh, sd = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(h2d: bool, d2h: bool) -> float:
+        cur = torch.cuda.current_stream()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        ev[0].record(cur)
+        for s_, on, pairs in ((sh, h2d, h2d_pairs), (sd, d2h, d2h_pairs)):
+            if not on:
+                continue
+            s_.wait_stream(cur)
+            with torch.cuda.stream(s_):
+                for _ in range(reps):
+                    for src, dst in pairs:
+                        dst.copy_(src, non_blocking=True)
+            cur.wait_stream(s_)
+        ev[1].record(cur)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / reps
+
+    run(True, True)    # warm-up
+    nb_h = sum(src.numel() * src.element_size() for src, _ in h2d_pairs)
+    nb_d = sum(src.numel() * src.element_size() for src, _ in d2h_pairs)
+    t_h, t_d, t_b = run(True, False), run(False, True), run(True, True)
+    return {"h2d_gbs": nb_h / (t_h * 1e-3) / 1e9, "d2h_gbs": nb_d / (t_d * 1e-3) / 1e9,
+            "h2d_ms": t_h, "d2h_ms": t_d, "both_ms": t_b}
 
 
 def bench_decode(args, dist, rb, pk):
@@ -364,41 +400,45 @@ def bench_parallel(args, dist, rb, pk):
                          "algorithmic_flops_per_launch": flops}}
 
 
-# fp32 FMA lanes: 148 SMs x 128 lanes, 2 flop per FMA, at the maximum SM clock
-FP32_LANES = 148 * 128
-
-
 def bench_backward(args, dist, rb, pk):
     w = inputs.BACKWARD
     q, k, v = inputs.qkv(w, "cuda")
     do = inputs.dout(w, "cuda")
     grads = tuple(torch.empty(w.b, w.H, w.N, d, dtype=torch.float32, device="cuda")
                   for d in (w.dk, w.dk, w.dv))
+    nbytes = rb.lib().retention_chunkwise_backward_workspace_bytes(w.b, w.H, w.N, w.dk, w.dv)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
     def step():
-        # one kernel: dq (forward scan), dk and dv (reverse scans) side by side
-        rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk, grads=grads)
+        # five tensor-core passes (dv, two dq halves, two dk halves) plus the reversed
+        # copies, state transposes and sums of the halves
+        rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk, grads=grads, workspace=ws)
 
-    steps = max(3, args.steps // 10)
+    def step_cuda_cores():
+        rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk, grads=grads,
+                                        cuda_cores=True)
+
+    steps = max(3, args.steps // 4)
     ms, _ = timed(step, steps, 3, dist)
     rb.check_device_error()
     ms_step = ms / steps
+    ms_cc, _ = timed(step_cuda_cores, 3, 1, dist)
+    rb.check_device_error()
     value, _ = aggregate(dist, ms, w.b * w.N * steps)
     flops = inputs.algorithmic_flops("backward", w)
     achieved = flops / (ms_step * 1e-3) / 1e12
-    peak = 2.0 * FP32_LANES * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
-    del q, k, v, do, grads
+    del q, k, v, do, grads, ws
     torch.cuda.empty_cache()
     return {"workload": f"{w.name}: gradient of chunkwise retention b{w.b} H{w.H} N{w.N} "
                         f"dk{w.dk} dv{w.dv} chunk {w.chunk}, bf16 q/k/v/dout N(0,1)/16, fp32 "
-                        "dq/dk/dv (retention_chunkwise_backward, CUDA-core kernel)",
+                        "dq/dk/dv (retention_chunkwise_backward_ws: tensor-core passes)",
             "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak,
-                         "traffic": profile_traffic("chunkwise_backward_blocked_backward.md",
-                                                    "simt_backward.cu"),
-                         "algorithmic_flops_per_launch": flops,
-                         "peak_basis": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x max SM clock"}}
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "traffic": profile_traffic("chunkwise_backward_tc_backward.md",
+                                                    "backward_tc.cu"),
+                         "algorithmic_flops_per_launch": flops},
+            "cuda_core_kernel_ms_per_step": ms_cc / 3}
 
 
 def bench_rglru(args, dist, rb, pk):
@@ -450,7 +490,8 @@ def bench_xpos(args, dist, rb, pk):
                         f"dk{w.dk}, bf16 in and out, theta_j = 10000^(-2j/dk), positions 0..N-1)",
             "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": profile_traffic("xpos_kernel_xpos.md", "xpos.cu"),
                          "algorithmic_bytes_per_launch": nbytes}}
 
 
@@ -509,6 +550,72 @@ def bench_sweep(args, dist, rb, pk):
             "points": points}
 
 
+MSR = dict(b=8, N=2048, D=4096, H=16, dk=256, dv=512, Dout=4096)
+
+
+def bench_msr_layer(args, dist, rb, pk):
+    """The gated multi-scale retention layer: four projections, the parallel form with all
+    three normalisations and the gated GroupNorm fused, the output projection."""
+    c = MSR
+    b, N, D, H, dk, dv, Do = c["b"], c["N"], c["D"], c["H"], c["dk"], c["dv"], c["Dout"]
+    x = inputs.randn((b, N, D), 8000, 1.0, "bf16", "cuda")
+    shapes = [(D, H * dk), (D, H * dk), (D, H * dv), (D, H * dv), (H * dv, Do)]
+    ws = [inputs.randn(sh, 8001 + i, sh[0] ** -0.5, "bf16", "cuda") for i, sh in enumerate(shapes)]
+    gam = inputs.gammas(H)
+    theta = [10000.0 ** (-j / (dk // 2)) for j in range(dk // 2)]
+    out = torch.empty(b, N, Do, dtype=torch.bfloat16, device="cuda")
+    wsb = torch.empty(rb.msr_layer_workspace_bytes(b, N, H, dk, dv, 0), dtype=torch.uint8,
+                      device="cuda")
+
+    def step():
+        rb.retention_msr_layer(x, *ws, gam, theta, flags=7, out=out, workspace=wsb)
+
+    steps = max(3, args.steps // 5)
+    ms, _ = timed(step, steps, 3, dist)
+    rb.check_device_error()
+    ms_step = ms / steps
+    value, _ = aggregate(dist, ms, b * N * steps)
+    proj = 2.0 * b * N * D * (2 * H * dk + 2 * H * dv) + 2.0 * b * N * H * dv * Do
+    core = float(b * H) * (dk + dv) * N * (N + 1)
+    flops = proj + core
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    del x, ws, out, wsb
+    torch.cuda.empty_cache()
+    return {"workload": f"msr_layer: gated multi-scale retention layer b{b} N{N} d_model{D} H{H} "
+                        f"dk{dk} dv{dv} d_out{Do}, bf16 x and weights N(0, 1/fan_in), xPos on Q/K "
+                        "fused into their projection, parallel form with all three "
+                        "normalisations + GroupNorm/swish gate fused, bf16 out "
+                        "(retention_msr_layer: six kernels)",
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "flops_split": {"projections": proj, "retention_core": core}}}
+
+
+def bench_gemm(args, dist, rb, pk):
+    """The layer's projection GEMM alone (C = A W, the V/G projection shape)."""
+    M, Nc, K = 16384, 8192, 4096
+    a = inputs.randn((M, K), 8100, 1.0, "bf16", "cuda")
+    w = inputs.randn((K, Nc), 8101, K ** -0.5, "bf16", "cuda")
+    c = torch.empty(M, Nc, dtype=torch.bfloat16, device="cuda")
+    steps = max(3, args.steps // 2)
+    ms, _ = timed(lambda: rb.retention_gemm(a, w, out=c), steps, 3, dist)
+    rb.check_device_error()
+    ms_step = ms / steps
+    flops = 2.0 * M * Nc * K
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    value, _ = aggregate(dist, ms, M * steps)
+    del a, w, c
+    torch.cuda.empty_cache()
+    return {"workload": f"gemm: projection GEMM C = A W, M{M} N{Nc} K{K}, bf16 in, fp32 "
+                        "accumulate, bf16 out (retention_gemm)",
+            "value": value, "unit": "rows/s", "ms_per_step": ms_step,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                         "algorithmic_flops_per_launch": flops}}
+
+
 def cpu_baseline_leg():
     w = inputs.CHUNKWISE_LONG
     threads = max(1, min(os.cpu_count() or 1, w.H))
@@ -520,7 +627,7 @@ def cpu_baseline_leg():
 # the legs reported beside the headline, in this order
 EXTRA_LEGS = {"decode": bench_decode, "parallel": bench_parallel, "backward": bench_backward,
               "rglru": bench_rglru, "xpos": bench_xpos, "chunkwise_bf16": bench_chunkwise_bf16,
-              "sweep": bench_sweep}
+              "sweep": bench_sweep, "msr_layer": bench_msr_layer, "gemm": bench_gemm}
 
 
 def run_ours(args, dist: Dist):
@@ -560,6 +667,7 @@ PROFILE_CASES = {
     "backward": "backward (b4 H16 N2048 dk256 dv512 chunk 64), bf16 in, fp32 gradients (1.1 GB)",
     "rglru": "rglru (b8 T4096 D4096), bf16 x and gates, fp32 y (1.3 GB)",
     "xpos": "xpos rotation of chunkwise_long's Q and K (b1 H16 N32768 dk256, bf16, 1.1 GB)",
+    "gemm": "projection GEMM M8192 N8192 K4096, bf16 in and out (0.2 GB)",
 }
 
 
@@ -586,14 +694,21 @@ def run_profile(case: str) -> int:
         do = inputs.dout(w, "cuda")
         grads = tuple(torch.empty(w.b, w.H, w.N, d, dtype=torch.float32, device="cuda")
                       for d in (w.dk, w.dk, w.dv))
+        nbytes = rb.lib().retention_chunkwise_backward_workspace_bytes(w.b, w.H, w.N, w.dk, w.dv)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         calls = [lambda: rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk,
-                                                         grads=grads)]
+                                                         grads=grads, workspace=ws)]
     elif case == "xpos":
         w = inputs.CHUNKWISE_LONG
         q, k, _ = inputs.qkv(w, "cuda")
         qo, ko = torch.empty_like(q), torch.empty_like(k)
         theta = [10000.0 ** (-j / (w.dk // 2)) for j in range(w.dk // 2)]
         calls = [lambda: rb.retention_xpos_rotate(q, k, theta, 0, q_out=qo, k_out=ko)]
+    elif case == "gemm":
+        a = inputs.randn((8192, 4096), 8100, 1.0, "bf16", "cuda")
+        w = inputs.randn((4096, 8192), 8101, 4096 ** -0.5, "bf16", "cuda")
+        cg = torch.empty(8192, 8192, dtype=torch.bfloat16, device="cuda")
+        calls = [lambda: rb.retention_gemm(a, w, out=cg)]
     elif case == "rglru":
         w = inputs.RGLRU
         x, ga, gx, lam = inputs.rglru_inputs(w, "cuda")

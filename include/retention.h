@@ -135,6 +135,34 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
                                  float* dstate_in, void* stream);
 
 /*
+ * retention_chunkwise_backward on tensor cores, with a caller workspace.  Every gradient
+ * above is itself a retention of the forward kind, so the call runs it as five passes of
+ * the pair-of-SMs chunkwise kernel (chunk 256; the result does not depend on the chunk):
+ *   grad_q = F(dout, v, k; S0^T),  grad_v = rev F(rev k, rev q, rev dout; dstate_out/gamma),
+ *   grad_k = rev F(rev v, rev dout, rev q; dstate_out^T/gamma),  dstate_in = gamma * (final
+ *   state of the grad_v pass),
+ * where F is eq.(7) with (q, k, v, state_in) replaced as written and rev reverses the
+ * token order; the 512-wide score dimension of the grad_q and grad_k passes runs as two
+ * 256-column halves whose outputs add.  Applies to bf16 inputs with dk = 256, dv a multiple
+ * of 256, N a multiple of 256 and every gamma in (0, 1] with gamma^(-256) <= 2^64;
+ * workspace (DEVICE, retention_chunkwise_backward_workspace_bytes(...) bytes, 256-byte
+ * aligned, owned by the caller) then holds reversed copies, partial outputs and states.
+ * Other shapes run the CUDA-core kernel of retention_chunkwise_backward and leave the
+ * workspace untouched (it may then be NULL).  Arguments, layouts and errors otherwise as
+ * retention_chunkwise_backward; a workspace that is too small returns RET_ERR_SHAPE.
+ */
+int retention_chunkwise_backward_ws(const void* q, const void* k, const void* v,
+                                    const void* dout, void* grad_q, void* grad_k, void* grad_v,
+                                    ret_dtype in_dtype, ret_dtype out_dtype, int b, int H,
+                                    int N, int dk, int dv, int chunk, const double* gamma,
+                                    const float* state_in, const float* dstate_out,
+                                    float* dstate_in, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* Workspace bytes of retention_chunkwise_backward_ws (0 for negative sizes).  Host-side. */
+size_t retention_chunkwise_backward_workspace_bytes(int b, int H, int N, int dk, int dv);
+
+/*
  * retention_chunkwise over HOST-resident inputs and outputs.  The sequence passes
  * through the device in segments of seg_len tokens (a multiple of chunk dividing N);
  * eq.(7) carries the state across any split at a chunk boundary ([RN2] "Retention" 3)),
@@ -397,7 +425,8 @@ enum {
     RET_KERNEL_CHUNKWISE_BACKWARD_SIMT = 9, /* chunkwise gradient, CUDA-core fp32 FMA   */
     RET_KERNEL_RGLRU = 10,          /* RG-LRU scan                                    */
     RET_KERNEL_XPOS = 11,           /* xPos rotation of Q and K                       */
-    RET_KERNEL_GEMM_TC = 12         /* projection GEMM of the layer, tensor cores     */
+    RET_KERNEL_GEMM_TC = 12,        /* projection GEMM of the layer, tensor cores     */
+    RET_KERNEL_CHUNKWISE_BACKWARD_TC = 13 /* chunkwise gradient as pair-kernel passes   */
 };
 
 /*

@@ -25,7 +25,8 @@ NORM_SCALE, NORM_DECAY, NORM_ROWSUM = 1, 2, 4
 NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
                 5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair",
-                9: "chunkwise_backward_simt", 10: "rglru", 11: "xpos", 12: "gemm_tc"}
+                9: "chunkwise_backward_simt", 10: "rglru", 11: "xpos", 12: "gemm_tc",
+                13: "chunkwise_backward_tc"}
 
 _lib = None
 _lock = threading.Lock()
@@ -61,6 +62,12 @@ def lib() -> ctypes.CDLL:
             L.retention_chunkwise.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, dp, vp, vp, vp]
             L.retention_chunkwise_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                                        i, i, i, dp, vp, vp, vp, vp]
+            L.retention_chunkwise_backward_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
+                                                          i, i, i, i, dp, vp, vp, vp, vp,
+                                                          ctypes.c_size_t, vp]
+            L.retention_chunkwise_backward_ws.restype = ctypes.c_int
+            L.retention_chunkwise_backward_workspace_bytes.argtypes = [i, i, i, i, i]
+            L.retention_chunkwise_backward_workspace_bytes.restype = ctypes.c_size_t
             L.retention_xpos_rotate.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, dp,
                                                 ctypes.c_longlong, vp]
             L.rglru_scan.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
@@ -193,11 +200,15 @@ def retention_chunkwise(q, k, v, gamma, chunk: int, state_in=None, state_out=Non
 
 def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None,
                                  dstate_out=None, dstate_in=None, grads=None,
-                                 out_dtype=torch.float32, stream=None):
+                                 out_dtype=torch.float32, stream=None, workspace=None,
+                                 cuda_cores: bool = False):
     """Gradient of retention_chunkwise for L = sum(dout * o) + <dstate_out, final state>.
 
     Returns (grad_q, grad_k, grad_v, dstate_in); dstate_in is None unless a tensor is
-    passed (fp32 [b,H,dk,dv]).  grads: optional preallocated (grad_q, grad_k, grad_v)."""
+    passed (fp32 [b,H,dk,dv]).  grads: optional preallocated (grad_q, grad_k, grad_v).
+    Runs retention_chunkwise_backward_ws (tensor-core passes where they apply; the
+    workspace is made here unless given); cuda_cores=True calls the CUDA-core
+    retention_chunkwise_backward instead."""
     b, H, N, dk = q.shape
     dv = v.shape[-1]
     if k.dtype != q.dtype or v.dtype != q.dtype or dout.dtype != q.dtype:
@@ -212,11 +223,29 @@ def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None
     gq, gk, gv = grads
     if gk.dtype != gq.dtype or gv.dtype != gq.dtype:
         raise TypeError("the three gradients must share one dtype")
-    rc = lib().retention_chunkwise_backward(
+    if cuda_cores:
+        rc = lib().retention_chunkwise_backward(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(gq), _ptr(gk), _ptr(gv),
+            _dtype_code(q.dtype), _dtype_code(gq.dtype), b, H, N, dk, dv, chunk,
+            _gamma(gamma, H), _ptr(state_in), _ptr(dstate_out), _ptr(dstate_in), _stream(stream))
+        _check("retention_chunkwise_backward", rc)
+        return gq, gk, gv, dstate_in
+    # the tensor-core passes need a workspace for the shapes they take (bf16, dk 256,
+    # dv and N multiples of 256); other shapes ignore it
+    owned = workspace is None and (q.dtype == torch.bfloat16 and dk == 256 and dv % 256 == 0
+                                   and N % 256 == 0)
+    if owned:
+        nbytes = int(lib().retention_chunkwise_backward_workspace_bytes(b, H, N, dk, dv))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    wptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    wbytes = ctypes.c_size_t(workspace.numel() if workspace is not None else 0)
+    rc = lib().retention_chunkwise_backward_ws(
         _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(gq), _ptr(gk), _ptr(gv),
         _dtype_code(q.dtype), _dtype_code(gq.dtype), b, H, N, dk, dv, chunk, _gamma(gamma, H),
-        _ptr(state_in), _ptr(dstate_out), _ptr(dstate_in), _stream(stream))
-    _check("retention_chunkwise_backward", rc)
+        _ptr(state_in), _ptr(dstate_out), _ptr(dstate_in), wptr, wbytes, _stream(stream))
+    if owned:
+        workspace.record_stream(stream or torch.cuda.current_stream(q.device))
+    _check("retention_chunkwise_backward_ws", rc)
     return gq, gk, gv, dstate_in
 
 

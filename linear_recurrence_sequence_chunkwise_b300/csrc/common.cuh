@@ -102,10 +102,13 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
 // Pair-of-SMs chunkwise kernel (cta_group::2): chunk 256, dk 256, dv a multiple of 128.
 // wait_ns bounds every on-chip wait (0: the default of 2 s); no_loads makes the TMA
 // producer issue nothing (self-test of the bounded waits: every wait then expires).
+// ldq, ldk, ldv, ldo: elements between rows of q, k, v and o (0: dk, dk, dv, dv), so that
+// column slices of wider matrices are read and written in place.
 cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,
-                                     cudaStream_t s, uint64_t wait_ns = 0, int no_loads = 0);
+                                     cudaStream_t s, uint64_t wait_ns = 0, int no_loads = 0,
+                                     int ldq = 0, int ldk = 0, int ldv = 0, int ldo = 0);
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
                                int out_bf16, int b, int H, int N, int dk, int dv,
                                const HeadConsts& hc, unsigned flags, cudaStream_t s);
@@ -114,6 +117,20 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
                                      int dk, int dv, const HeadConsts& hc, unsigned flags,
                                      float eps, const float* weight, const float* bias,
                                      cudaStream_t s);
+// Gradient of the chunkwise form as five pair-kernel passes (backward_tc.cu): bf16 inputs,
+// dk 256, dv a multiple of 256, N a multiple of 256, decays the pair kernel takes at chunk
+// 256 (hc256: head constants for chunk 256).  workspace: chunkwise_backward_tc_workspace
+// bytes, 256-byte aligned.
+bool chunkwise_pair_supported(int dk, int dv, int chunk, const HeadConsts& hc, int H);
+bool chunkwise_backward_tc_supported(int in_bf16, int H, int N, int dk, int dv,
+                                     const HeadConsts& hc256);
+size_t chunkwise_backward_tc_workspace(int b, int H, int N, int dk, int dv);
+cudaError_t launch_chunkwise_backward_tc(const void* q, const void* k, const void* v,
+                                         const void* dout, void* grad_q, void* grad_k,
+                                         void* grad_v, int out_bf16, int b, int H, int N, int dk,
+                                         int dv, const HeadConsts& hc256, const float* state_in,
+                                         const float* dstate_out, float* dstate_in,
+                                         void* workspace, cudaStream_t s);
 // Count one successful kernel launch (host-side, process-wide) and record its
 // RET_KERNEL_* code for the launching host thread.
 void count_launch(int kernel_code);

@@ -228,6 +228,51 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
         H, N, dk, dv, kchunk, hc, state_in, dstate_out, dstate_in, s));
 }
 
+size_t retention_chunkwise_backward_workspace_bytes(int b, int H, int N, int dk, int dv) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return 0;
+    return ret::chunkwise_backward_tc_workspace(b, H, N, dk, dv);
+}
+
+int retention_chunkwise_backward_ws(const void* q, const void* k, const void* v,
+                                    const void* dout, void* grad_q, void* grad_k, void* grad_v,
+                                    ret_dtype in_dtype, ret_dtype out_dtype, int b, int H,
+                                    int N, int dk, int dv, int chunk, const double* gamma,
+                                    const float* state_in, const float* dstate_out,
+                                    float* dstate_in, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+    // the checks of retention_chunkwise_backward first (it also handles every case the
+    // tensor-core passes do not take)
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return RET_ERR_SHAPE;
+    if (!is_dtype(in_dtype) || !is_dtype(out_dtype)) return RET_ERR_DTYPE;
+    if (!dims_ok(dk, dv)) return RET_ERR_UNSUPPORTED;
+    if (chunk < 16 || chunk > 256 || chunk % 16 != 0) return RET_ERR_SHAPE;
+    if (N % chunk != 0) return RET_ERR_SHAPE;
+    if (b == 0 || H == 0 || N == 0 || !gamma || H > ret::kMaxHeads)
+        return retention_chunkwise_backward(q, k, v, dout, grad_q, grad_k, grad_v, in_dtype,
+                                            out_dtype, b, H, N, dk, dv, chunk, gamma, state_in,
+                                            dstate_out, dstate_in, stream);
+    HeadConsts hc256;
+    int rc = head_consts(gamma, H, 256, &hc256);
+    if (rc != RET_OK) return rc;
+    if (!ret::chunkwise_backward_tc_supported(in_dtype == RET_BF16, H, N, dk, dv, hc256))
+        return retention_chunkwise_backward(q, k, v, dout, grad_q, grad_k, grad_v, in_dtype,
+                                            out_dtype, b, H, N, dk, dv, chunk, gamma, state_in,
+                                            dstate_out, dstate_in, stream);
+    if (!q || !k || !v || !dout || !grad_q || !grad_k || !grad_v || !workspace) return RET_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) ||
+        !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RET_ERR_ALIGN;
+    if ((state_in && !aligned16(state_in)) || (dstate_out && !aligned16(dstate_out)) ||
+        (dstate_in && !aligned16(dstate_in)))
+        return RET_ERR_ALIGN;
+    if (workspace_bytes < ret::chunkwise_backward_tc_workspace(b, H, N, dk, dv)) return RET_ERR_SHAPE;
+    if ((long long)b * H * N >= (1LL << 31)) return RET_ERR_UNSUPPORTED;
+    return cuda_status(ret::launch_chunkwise_backward_tc(
+        q, k, v, dout, grad_q, grad_k, grad_v, out_dtype == RET_BF16, b, H, N, dk, dv, hc256,
+        state_in, dstate_out, dstate_in, workspace, static_cast<cudaStream_t>(stream)));
+}
+
 int retention_recurrent_step(const void* q, const void* k, const void* v, float* state, void* o,
                              ret_dtype in_dtype, ret_dtype out_dtype, int b, int H, int dk,
                              int dv, const double* gamma, void* stream) {

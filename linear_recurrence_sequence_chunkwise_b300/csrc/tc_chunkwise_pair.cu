@@ -155,7 +155,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                       void* __restrict__ out_base, const float* __restrict__ state_in,
                       float* __restrict__ state_out, int N,
                       int H, int dv, int fp16_first, const Decay dc, uint64_t wait_ns,
-                      int no_loads) {
+                      int no_loads, int ldo) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = sm + kQOff;
@@ -493,10 +493,10 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                             uint4* dst;
                             if (OUT_BF16)
                                 dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
-                                                               (row0 + k) * dv + col) + p8;
+                                                               (row0 + k) * ldo + col) + p8;
                             else
                                 dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) +
-                                                               (row0 + k) * dv + col) + p8;
+                                                               (row0 + k) * ldo + col) + p8;
                             *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
                         }
                     }
@@ -755,9 +755,16 @@ bool chunkwise_pair_supported(int dk, int dv, int chunk, const HeadConsts& hc, i
 cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,
-                                     cudaStream_t s, uint64_t wait_ns, int no_loads) {
+                                     cudaStream_t s, uint64_t wait_ns, int no_loads, int ldq,
+                                     int ldk, int ldv, int ldo) {
     if (!chunkwise_pair_supported(dk, dv, chunk, hc, H)) return cudaErrorNotSupported;
     if (wait_ns == 0) wait_ns = kWaitLimitNs;
+    if (ldq == 0) ldq = dk;
+    if (ldk == 0) ldk = dk;
+    if (ldv == 0) ldv = dv;
+    if (ldo == 0) ldo = dv;
+    if (ldq < dk || ldk < dk || ldv < dv || ldo < dv || (ldq | ldk | ldv | ldo) % 8 != 0)
+        return cudaErrorInvalidValue;
     Decay dc;
     int fp16_first = 1;
     for (int h = 0; h < H; ++h) {
@@ -771,8 +778,9 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     const long long rows = (long long)b * H * N;
     if (rows >= (1LL << 31)) return cudaErrorNotSupported;
     CUtensorMap mq, mk, mv;
-    if (!make_map_bf16(&mq, q, rows, dk, 128) || !make_map_bf16(&mk, k, rows, dk, 128) ||
-        !make_map_bf16(&mv, v, rows, dv, 128))
+    if (!make_map_bf16_pitch(&mq, q, rows, dk, ldq, 128) ||
+        !make_map_bf16_pitch(&mk, k, rows, dk, ldk, 128) ||
+        !make_map_bf16_pitch(&mv, v, rows, dv, ldv, 128))
         return cudaErrorInvalidValue;
     const long long grid = 2LL * b * H * (dv / 128);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -781,7 +789,7 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv,
-                                                fp16_first, dc, wait_ns, no_loads);
+                                                fp16_first, dc, wait_ns, no_loads, ldo);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
     return e;

@@ -40,6 +40,22 @@ inline bool make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uin
            CUDA_SUCCESS;
 }
 
+// As make_map_bf16 for rows `pitch` elements apart (pitch >= cols, pitch * 2 bytes a
+// multiple of 16): a column slice of a wider row-major matrix.
+inline bool make_map_bf16_pitch(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                uint64_t pitch, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Map over a bf16 tensor [planes][rows][cols] (cols * 2 bytes a multiple of 16),
 // loading boxes of 64 columns by box_rows rows of one plane with the 128-byte
 // swizzle.  Rows past `rows` in a plane read as zero.

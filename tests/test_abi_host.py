@@ -42,7 +42,8 @@ def test_exports_every_declared_function(L):
                           "retention_xpos_rotate", "retention_chunkwise_format_reruns",
                           "retention_chunkwise_wait_selftest", "retention_msr_layer",
                           "retention_msr_layer_workspace_bytes", "retention_gemm",
-                          "retention_project_heads"}
+                          "retention_project_heads", "retention_chunkwise_backward_ws",
+                          "retention_chunkwise_backward_workspace_bytes"}
     for n in names:
         assert getattr(L, n) is not None
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,

@@ -38,15 +38,22 @@ def make(b, H, N, dk, dv, seed, dtype="f32", std=1.0, states=True):
     return q, k, v, do, s0, ds
 
 
-def run(q, k, v, do, gamma, chunk, s0=None, ds=None, out_dtype=torch.float32):
-    b, H, _, dk = q.shape
+def tc_applies(q, gamma, dk, dv, N):
+    """The shapes retention_chunkwise_backward_ws runs as tensor-core passes."""
+    return (q.dtype == torch.bfloat16 and dk == 256 and dv % 256 == 0 and N % 256 == 0
+            and all(0.0 < g and g ** -256 <= 2.0 ** 64 for g in gamma))
+
+
+def run(q, k, v, do, gamma, chunk, s0=None, ds=None, out_dtype=torch.float32, cuda_cores=False):
+    b, H, N, dk = q.shape
     dv = v.shape[-1]
     di = torch.full((b, H, dk, dv), float("nan"), device=DEV)
     gq, gk, gv, di = rb.retention_chunkwise_backward(q, k, v, do, gamma, chunk, state_in=s0,
                                                      dstate_out=ds, dstate_in=di,
-                                                     out_dtype=out_dtype)
+                                                     out_dtype=out_dtype, cuda_cores=cuda_cores)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == "chunkwise_backward_simt"
+    tc = not cuda_cores and tc_applies(q, gamma, dk, dv, N)
+    assert rb.last_kernel() == ("chunkwise_backward_tc" if tc else "chunkwise_backward_simt")
     return gq, gk, gv, di
 
 
@@ -135,7 +142,7 @@ def test_full_size_training_shape_sampled():
     do = inputs.dout(w, DEV)
     gq, gk, gv, _ = rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == "chunkwise_backward_simt"
+    assert rb.last_kernel() == "chunkwise_backward_tc"
     idx = [(0, 0), (3, 15)]
     us = [(bi, h) + tuple(t[bi:bi + 1, h:h + 1].cpu() for t in (q, k, v, do)) for bi, h in idx]
     outs = oracle.map_units(
@@ -144,3 +151,32 @@ def test_full_size_training_shape_sampled():
     for (bi, h, *_), want in zip(us, outs):
         for name, g, wnt in zip(("dq", "dk", "dv"), (gq, gk, gv), want[:3]):
             assert err_bf16(g[bi:bi + 1, h:h + 1], wnt) < TOL_BF16, (bi, h, name)
+
+
+# Tensor-core passes (retention_chunkwise_backward_ws): bf16, dk 256, dv 256 or 512.
+@pytest.mark.parametrize("dv,N,states", [(512, 512, True), (256, 768, True), (512, 256, False)])
+def test_tensor_core_passes_against_the_oracle(dv, N, states):
+    b, H, dk = 2, 2, 256
+    gamma = [inputs.gammas(16)[0], 1.0 - 2.0 ** -12]
+    q, k, v, do, s0, ds = make(b, H, N, dk, dv, 800 + dv + N, "bf16", 1 / 16, states=states)
+    got = run(q, k, v, do, gamma, 64, s0, ds)
+    want = oracle.chunkwise_backward(q, k, v, do, gamma, state_in=s0, dstate_out=ds)
+    for name, g, w in zip(("dq", "dk", "dv", "dstate_in"), got, want):
+        assert err_bf16(g, w) < TOL_BF16, name
+    rb.check_device_error()
+
+
+def test_tensor_core_passes_match_the_cuda_core_kernel_and_bf16_grads():
+    b, H, N, dk, dv = 1, 2, 512, 256, 512
+    gamma = [0.97, 0.995]
+    q, k, v, do, s0, ds = make(b, H, N, dk, dv, 850, "bf16", 1 / 16)
+    tc = run(q, k, v, do, gamma, 128, s0, ds)
+    cc = run(q, k, v, do, gamma, 128, s0, ds, cuda_cores=True)
+    for name, a, c in zip(("dq", "dk", "dv", "dstate_in"), tc, cc):
+        assert err_bf16(a, c) < TOL_BF16, name
+    want = oracle.chunkwise_backward(q, k, v, do, gamma, state_in=s0, dstate_out=ds)
+    g16 = run(q, k, v, do, gamma, 128, s0, ds, out_dtype=torch.bfloat16)
+    for g, w in zip(g16[:3], want[:3]):
+        assert g.dtype == torch.bfloat16
+        assert err_bf16_out(g, w) <= 1.0
+    rb.check_device_error()
