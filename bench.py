@@ -320,14 +320,15 @@ def host_link(h2d_pairs, d2h_pairs, reps: int = 3) -> dict:
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         torch.cuda.synchronize()
         ev[0].record(cur)
-        for s_, on, pairs in ((sh, h2d, h2d_pairs), (sd, d2h, d2h_pairs)):
-            if not on:
-                continue
+        jobs = [(s_, pairs) for s_, on, pairs in ((sh, h2d, h2d_pairs), (sd, d2h, d2h_pairs)) if on]
+        for s_, _ in jobs:          # both copy streams start from the same point
             s_.wait_stream(cur)
+        for s_, pairs in jobs:
             with torch.cuda.stream(s_):
                 for _ in range(reps):
                     for src, dst in pairs:
                         dst.copy_(src, non_blocking=True)
+        for s_, _ in jobs:
             cur.wait_stream(s_)
         ev[1].record(cur)
         torch.cuda.synchronize()
@@ -406,12 +407,12 @@ def bench_backward(args, dist, rb, pk):
     do = inputs.dout(w, "cuda")
     grads = tuple(torch.empty(w.b, w.H, w.N, d, dtype=torch.float32, device="cuda")
                   for d in (w.dk, w.dk, w.dv))
-    nbytes = rb.lib().retention_chunkwise_backward_workspace_bytes(w.b, w.H, w.N, w.dk, w.dv)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    nbytes = rb.backward_workspace_bytes(torch.float32, w.b, w.H, w.N, w.dk, w.dv)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
 
     def step():
-        # five tensor-core passes (dv, two dq halves, two dk halves) plus the reversed
-        # copies, state transposes and sums of the halves
+        # five tensor-core passes: dv in reversed time on the caller's stream, the two dq
+        # halves and the two dk halves (reversed time) as chains on two side streams
         rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk, grads=grads, workspace=ws)
 
     def step_cuda_cores():
@@ -694,8 +695,8 @@ def run_profile(case: str) -> int:
         do = inputs.dout(w, "cuda")
         grads = tuple(torch.empty(w.b, w.H, w.N, d, dtype=torch.float32, device="cuda")
                       for d in (w.dk, w.dk, w.dv))
-        nbytes = rb.lib().retention_chunkwise_backward_workspace_bytes(w.b, w.H, w.N, w.dk, w.dv)
-        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        nbytes = rb.backward_workspace_bytes(torch.float32, w.b, w.H, w.N, w.dk, w.dv)
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
         calls = [lambda: rb.retention_chunkwise_backward(q, k, v, do, w.gamma, w.chunk,
                                                          grads=grads, workspace=ws)]
     elif case == "xpos":

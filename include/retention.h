@@ -136,17 +136,24 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
 
 /*
  * retention_chunkwise_backward on tensor cores, with a caller workspace.  Every gradient
- * above is itself a retention of the forward kind, so the call runs it as five passes of
- * the pair-of-SMs chunkwise kernel (chunk 256; the result does not depend on the chunk):
- *   grad_q = F(dout, v, k; S0^T),  grad_v = rev F(rev k, rev q, rev dout; dstate_out/gamma),
- *   grad_k = rev F(rev v, rev dout, rev q; dstate_out^T/gamma),  dstate_in = gamma * (final
- *   state of the grad_v pass),
- * where F is eq.(7) with (q, k, v, state_in) replaced as written and rev reverses the
- * token order; the 512-wide score dimension of the grad_q and grad_k passes runs as two
- * 256-column halves whose outputs add.  Applies to bf16 inputs with dk = 256, dv a multiple
- * of 256, N a multiple of 256 and every gamma in (0, 1] with gamma^(-256) <= 2^64;
- * workspace (DEVICE, retention_chunkwise_backward_workspace_bytes(...) bytes, 256-byte
- * aligned, owned by the caller) then holds reversed copies, partial outputs and states.
+ * above is itself a retention of the forward kind, so the call runs it as passes of the
+ * pair-of-SMs chunkwise kernel (chunk 256; the result does not depend on the chunk):
+ *   grad_q = F(dout, v, k; S0^T),  grad_v = R(k, q, dout; dstate_out/gamma),
+ *   grad_k = R(v, dout, q; dstate_out^T/gamma),  dstate_in = gamma * (final state of the
+ *   grad_v pass),
+ * where F is eq.(7) with (q, k, v, state_in) replaced as written and R is eq.(7) in
+ * reversed time (row n collects the rows m >= n with gamma^(m-n), the state entering at
+ * the end of the sequence).  The dv-wide score dimension of the grad_q and grad_k passes
+ * runs as 256-column slices whose outputs add inside the kernel.  The grad_v pass and the
+ * grad_q and grad_k chains run concurrently: on stream and on two side streams that the
+ * library makes on the first call on a device (make that call before capturing stream
+ * into a graph) and keeps; stream waits for both before the call returns, also on an
+ * error, and the library creates and releases three CUDA events per call.
+ * Applies to bf16 inputs with dk = 256, dv a multiple of 256, N a multiple of 256 and
+ * every gamma in (0, 1] with gamma^(-256) <= 2^64; workspace (DEVICE,
+ * retention_chunkwise_backward_workspace_bytes(out_dtype, ...) bytes, 256-byte aligned,
+ * owned by the caller and not touched by anything else until stream reaches this call's
+ * end) then holds the transposed states and, for bf16 gradients, fp32 partial sums.
  * Other shapes run the CUDA-core kernel of retention_chunkwise_backward and leave the
  * workspace untouched (it may then be NULL).  Arguments, layouts and errors otherwise as
  * retention_chunkwise_backward; a workspace that is too small returns RET_ERR_SHAPE.
@@ -159,8 +166,10 @@ int retention_chunkwise_backward_ws(const void* q, const void* k, const void* v,
                                     float* dstate_in, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
-/* Workspace bytes of retention_chunkwise_backward_ws (0 for negative sizes).  Host-side. */
-size_t retention_chunkwise_backward_workspace_bytes(int b, int H, int N, int dk, int dv);
+/* Workspace bytes of retention_chunkwise_backward_ws for gradients of out_dtype (0 for
+ * negative sizes and for shapes the tensor-core passes do not take).  Host-side. */
+size_t retention_chunkwise_backward_workspace_bytes(ret_dtype out_dtype, int b, int H, int N,
+                                                    int dk, int dv);
 
 /*
  * retention_chunkwise over HOST-resident inputs and outputs.  The sequence passes

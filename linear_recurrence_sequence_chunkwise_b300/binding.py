@@ -66,7 +66,7 @@ def lib() -> ctypes.CDLL:
                                                           i, i, i, i, dp, vp, vp, vp, vp,
                                                           ctypes.c_size_t, vp]
             L.retention_chunkwise_backward_ws.restype = ctypes.c_int
-            L.retention_chunkwise_backward_workspace_bytes.argtypes = [i, i, i, i, i]
+            L.retention_chunkwise_backward_workspace_bytes.argtypes = [i, i, i, i, i, i]
             L.retention_chunkwise_backward_workspace_bytes.restype = ctypes.c_size_t
             L.retention_xpos_rotate.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, dp,
                                                 ctypes.c_longlong, vp]
@@ -198,6 +198,13 @@ def retention_chunkwise(q, k, v, gamma, chunk: int, state_in=None, state_out=Non
     return out
 
 
+def backward_workspace_bytes(out_dtype, b: int, H: int, N: int, dk: int, dv: int) -> int:
+    """Workspace bytes of retention_chunkwise_backward_ws (0 where the tensor-core passes
+    do not apply)."""
+    return int(lib().retention_chunkwise_backward_workspace_bytes(_dtype_code(out_dtype), b, H,
+                                                                  N, dk, dv))
+
+
 def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None,
                                  dstate_out=None, dstate_in=None, grads=None,
                                  out_dtype=torch.float32, stream=None, workspace=None,
@@ -235,7 +242,7 @@ def retention_chunkwise_backward(q, k, v, dout, gamma, chunk: int, state_in=None
     owned = workspace is None and (q.dtype == torch.bfloat16 and dk == 256 and dv % 256 == 0
                                    and N % 256 == 0)
     if owned:
-        nbytes = int(lib().retention_chunkwise_backward_workspace_bytes(b, H, N, dk, dv))
+        nbytes = backward_workspace_bytes(gq.dtype, b, H, N, dk, dv)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     wptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
     wbytes = ctypes.c_size_t(workspace.numel() if workspace is not None else 0)

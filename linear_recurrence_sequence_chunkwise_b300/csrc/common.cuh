@@ -11,6 +11,7 @@
 namespace ret {
 
 constexpr int kMaxHeads = 128;
+constexpr int kMaxDevices = 64;   // per-device caches of the host code
 
 // Per-head decay constants, computed on the host in fp64 and rounded once.
 //   l2g  = log2(gamma)            (-inf for gamma = 0)
@@ -103,12 +104,16 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
 // wait_ns bounds every on-chip wait (0: the default of 2 s); no_loads makes the TMA
 // producer issue nothing (self-test of the bounded waits: every wait then expires).
 // ldq, ldk, ldv, ldo: elements between rows of q, k, v and o (0: dk, dk, dv, dv), so that
-// column slices of wider matrices are read and written in place.
+// column slices of wider matrices are read and written in place.  rev != 0 runs eq.(7) in
+// reversed time on the rows as stored (row n collects the keys m >= n with g^(m-n); the
+// chunks are scanned from the last; state_in enters at the end, state_out leaves at the
+// start).  acc (fp32, pitch ldo, may equal o when o is fp32) is added to the output.
 cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,
                                      cudaStream_t s, uint64_t wait_ns = 0, int no_loads = 0,
-                                     int ldq = 0, int ldk = 0, int ldv = 0, int ldo = 0);
+                                     int ldq = 0, int ldk = 0, int ldv = 0, int ldo = 0,
+                                     int rev = 0, const float* acc = nullptr);
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o,
                                int out_bf16, int b, int H, int N, int dk, int dv,
                                const HeadConsts& hc, unsigned flags, cudaStream_t s);
@@ -117,20 +122,24 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
                                      int dk, int dv, const HeadConsts& hc, unsigned flags,
                                      float eps, const float* weight, const float* bias,
                                      cudaStream_t s);
-// Gradient of the chunkwise form as five pair-kernel passes (backward_tc.cu): bf16 inputs,
+// Gradient of the chunkwise form as pair-kernel passes (backward_tc.cu): bf16 inputs,
 // dk 256, dv a multiple of 256, N a multiple of 256, decays the pair kernel takes at chunk
 // 256 (hc256: head constants for chunk 256).  workspace: chunkwise_backward_tc_workspace
 // bytes, 256-byte aligned.
 bool chunkwise_pair_supported(int dk, int dv, int chunk, const HeadConsts& hc, int H);
 bool chunkwise_backward_tc_supported(int in_bf16, int H, int N, int dk, int dv,
                                      const HeadConsts& hc256);
-size_t chunkwise_backward_tc_workspace(int b, int H, int N, int dk, int dv);
+size_t chunkwise_backward_tc_workspace(int out_bf16, int b, int H, int N, int dk, int dv);
 cudaError_t launch_chunkwise_backward_tc(const void* q, const void* k, const void* v,
                                          const void* dout, void* grad_q, void* grad_k,
                                          void* grad_v, int out_bf16, int b, int H, int N, int dk,
                                          int dv, const HeadConsts& hc256, const float* state_in,
                                          const float* dstate_out, float* dstate_in,
                                          void* workspace, cudaStream_t s);
+// The current CUDA context (driver entry point fetched through the runtime, so the
+// library needs no link to libcuda); nullptr if it cannot be queried.  Per-device caches
+// compare it to notice a context made after a device reset.
+void* current_context();
 // Count one successful kernel launch (host-side, process-wide) and record its
 // RET_KERNEL_* code for the launching host thread.
 void count_launch(int kernel_code);

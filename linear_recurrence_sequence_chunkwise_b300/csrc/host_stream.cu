@@ -77,10 +77,39 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int i
 constexpr size_t kStaticScratchBytes = size_t(48) << 20;
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
+// Device address of g_static_scratch on the current device, looked up once per device
+// and context: after cudaDeviceReset the module loads again in a new context, possibly at
+// another address, so a changed context triggers a new lookup.
+cudaError_t static_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[ret::kMaxDevices] = {};
+    static void* ctx[ret::kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= ret::kMaxDevices) return cudaErrorInvalidDevice;
+    // cudaFree(0) makes the device's primary context current if no context is yet
+    e = cudaFree(nullptr);
+    if (e != cudaSuccess) return e;
+    void* const cur = ret::current_context();
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev] || !cur || cur != ctx[dev]) {
+        e = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
+        if (e != cudaSuccess) {
+            addr[dev] = nullptr;
+            ctx[dev] = nullptr;
+            return e;
+        }
+        ctx[dev] = cur;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
 
-// The current CUDA context (driver entry point fetched through the runtime, so the
-// library needs no link to libcuda); nullptr if it cannot be queried.
+}  // namespace
+
+namespace ret {
+
 void* current_context() {
     using Fn = CUresult (*)(CUcontext*);
     static Fn fn = [] {
@@ -97,36 +126,7 @@ void* current_context() {
     return c;
 }
 
-// Device address of g_static_scratch on the current device, looked up once per device
-// and context: after cudaDeviceReset the module loads again in a new context, possibly at
-// another address, so a changed context triggers a new lookup.
-cudaError_t static_scratch(void** out) {
-    static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
-    static void* ctx[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    // cudaFree(0) makes the device's primary context current if no context is yet
-    e = cudaFree(nullptr);
-    if (e != cudaSuccess) return e;
-    void* const cur = current_context();
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev] || !cur || cur != ctx[dev]) {
-        e = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
-        if (e != cudaSuccess) {
-            addr[dev] = nullptr;
-            ctx[dev] = nullptr;
-            return e;
-        }
-        ctx[dev] = cur;
-    }
-    *out = addr[dev];
-    return cudaSuccess;
-}
-
-}  // namespace
+}  // namespace ret
 
 extern "C" {
 

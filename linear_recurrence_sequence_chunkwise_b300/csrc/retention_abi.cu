@@ -228,9 +228,10 @@ int retention_chunkwise_backward(const void* q, const void* k, const void* v,
         H, N, dk, dv, kchunk, hc, state_in, dstate_out, dstate_in, s));
 }
 
-size_t retention_chunkwise_backward_workspace_bytes(int b, int H, int N, int dk, int dv) {
-    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0) return 0;
-    return ret::chunkwise_backward_tc_workspace(b, H, N, dk, dv);
+size_t retention_chunkwise_backward_workspace_bytes(ret_dtype out_dtype, int b, int H, int N,
+                                                    int dk, int dv) {
+    if (b < 0 || H < 0 || N < 0 || dk < 0 || dv < 0 || dk != 256 || dv % 256 != 0) return 0;
+    return ret::chunkwise_backward_tc_workspace(out_dtype == RET_BF16, b, H, N, dk, dv);
 }
 
 int retention_chunkwise_backward_ws(const void* q, const void* k, const void* v,
@@ -266,7 +267,8 @@ int retention_chunkwise_backward_ws(const void* q, const void* k, const void* v,
     if ((state_in && !aligned16(state_in)) || (dstate_out && !aligned16(dstate_out)) ||
         (dstate_in && !aligned16(dstate_in)))
         return RET_ERR_ALIGN;
-    if (workspace_bytes < ret::chunkwise_backward_tc_workspace(b, H, N, dk, dv)) return RET_ERR_SHAPE;
+    if (workspace_bytes < ret::chunkwise_backward_tc_workspace(out_dtype == RET_BF16, b, H, N, dk, dv))
+        return RET_ERR_SHAPE;
     if ((long long)b * H * N >= (1LL << 31)) return RET_ERR_UNSUPPORTED;
     return cuda_status(ret::launch_chunkwise_backward_tc(
         q, k, v, dout, grad_q, grad_k, grad_v, out_dtype == RET_BF16, b, H, N, dk, dv, hc256,

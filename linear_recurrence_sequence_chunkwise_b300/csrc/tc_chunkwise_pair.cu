@@ -148,14 +148,14 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
 }
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool ACC>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                       const __grid_constant__ CUtensorMap mv,
                       void* __restrict__ out_base, const float* __restrict__ state_in,
                       float* __restrict__ state_out, int N,
                       int H, int dv, int fp16_first, const Decay dc, uint64_t wait_ns,
-                      int no_loads, int ldo) {
+                      int no_loads, int ldo, int rev, const float* __restrict__ acc) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = sm + kQOff;
@@ -242,7 +242,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 // the pairs of one head share Q and K: pull the next chunk's boxes into L2
                 auto prefetch = [&](int c) {
                     if (c >= nchunks) return;
-                    const int r0 = rowbase + c * kB;
+                    const int r0 = rowbase + (rev ? nchunks - 1 - c : c) * kB;
                     for (int a = 0; a < 4; ++a) {
                         tma_prefetch_l2(&mq, 64 * a, r0 + own);
                         tma_prefetch_l2(&mk, 64 * a, r0 + own);
@@ -254,7 +254,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 if (no_loads) ok = false;
                 if (ok) prefetch(0);
                 for (int c = 0; c < nchunks && ok; ++c) {
-                    const int r0 = rowbase + c * kB;
+                    const int r0 = rowbase + (rev ? nchunks - 1 - c : c) * kB;
                     // Q: own query rows, all dk (after the previous chunk's Q.R)
                     if (c > 0 && !w(&bars.q_empty, par(c - 1))) break;
                     if (rank == 0) { mbar_arrive_expect_tx(&bars.q_full, 2 * 4 * kBox); ++armed_q; }
@@ -436,26 +436,46 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 // ---------------------------------------------- scores -> P, then output
                 const int half = (warp - kFirstP) >> 2;  // key half (P) / 64-column half (O)
                 const float sa = dc.a[head];
-                // P = a S with the causal mask (key > j is zero).  Key quarter qq (32 keys)
-                // is below this warp's rows for qq < dq, holds their diagonal for qq = dq and
-                // lies after them for qq > dq (all zero): warp-uniform.
+                // P = a S with the causal mask (key > j is zero; reversed: key < j).  Key
+                // quarter qq (32 keys) holds the diagonal of this warp's rows for qq = dq; the
+                // quarters on the far side of it are all zero (warp-uniform).
                 const int dq = 4 * (int)rank + q4;
                 float pmax = 0.f;
+                auto live = [&](int qq) { return rev ? qq >= dq : qq <= dq; };
                 auto scaled = [&](const float* x, int qq, int e) {
                     const int kc = 32 * qq + e;
-                    return (qq < dq || kc <= j) ? x[e] * sa : 0.f;
+                    return (qq != dq || (rev ? kc >= j : kc <= j)) ? x[e] * sa : 0.f;
                 };
-                const float xi = exp2f(l2g * ((float)(j + 1) - 0.5f * (float)kB));
+                // xi_j = g^(j+1-B/2); reversed, row j stands at position B-1-j
+                const float xi = exp2f(l2g * (rev ? 0.5f * (float)kB - (float)j
+                                                  : (float)(j + 1) - 0.5f * (float)kB));
                 // output rows of chunk c: xi_j * O for this warp's 64 columns, straight from
                 // registers.  Each 128-byte row segment (32 fp32 or 64 bf16 columns = 8 items
                 // of 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so
                 // that every store instruction writes four whole 128-byte segments.  The last
                 // TMEM read releases O for the next Q.R.
+                // acc (optional, fp32, pitch ldo): added to the output (in place when acc is
+                // the output); each thread reads its own row's columns before the transpose.
+                auto row_of = [&](int c) {
+                    return (size_t)bh * N + (size_t)(rev ? nchunks - 1 - c : c) * kB;
+                };
+                auto add_acc = [&](float* o, int c, size_t col0) {
+                    const float4* ap = reinterpret_cast<const float4*>(acc + (row_of(c) + j) * ldo + col0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 t = ap[e];
+                        o[4 * e] = fmaf(xi, o[4 * e], t.x);
+                        o[4 * e + 1] = fmaf(xi, o[4 * e + 1], t.y);
+                        o[4 * e + 2] = fmaf(xi, o[4 * e + 2], t.z);
+                        o[4 * e + 3] = fmaf(xi, o[4 * e + 3], t.w);
+                    }
+                };
                 auto do_out = [&](int c) {
                     if (!wait(&bars.o_full, par(c))) return;
                     tc_fence_after();
                     const int p8 = lane & 7;
-                    const size_t row0 = (size_t)bh * N + (size_t)c * kB + (size_t)(j - p8);
+                    const size_t row0 = row_of(c) + (size_t)(j - p8);
+                    const size_t colh = (size_t)blk * 128 + (size_t)(64 * half);
                     constexpr int kSegs = OUT_BF16 ? 1 : 2;       // 128-byte segments per 64 columns
                     constexpr int kSegCols = OUT_BF16 ? 64 : 32;
 #pragma unroll 1
@@ -469,22 +489,39 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                                 tmem_ld32(tc0 + 32 * hh, o);
                                 tmem_wait_ld();
                                 if (hh == 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+                                if (ACC) {
+                                    add_acc(o, c, colh + 32 * hh);
 #pragma unroll
-                                for (int k = 0; k < 4; ++k)
+                                    for (int k = 0; k < 4; ++k)
 #pragma unroll
-                                    for (int w = 0; w < 4; ++w)
-                                        a[4 * hh + k][w] =
-                                            pack_bf16(xi * o[8 * k + 2 * w], xi * o[8 * k + 2 * w + 1]);
+                                        for (int w = 0; w < 4; ++w)
+                                            a[4 * hh + k][w] = pack_bf16(o[8 * k + 2 * w], o[8 * k + 2 * w + 1]);
+                                } else {
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                                        for (int w = 0; w < 4; ++w)
+                                            a[4 * hh + k][w] = pack_bf16(xi * o[8 * k + 2 * w],
+                                                                         xi * o[8 * k + 2 * w + 1]);
+                                }
                             }
                         } else {
                             float o[32];
                             tmem_ld32(tc0, o);
                             tmem_wait_ld();
                             if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
+                            if (ACC) {
+                                add_acc(o, c, colh + kSegCols * sg);
 #pragma unroll
-                            for (int k = 0; k < 8; ++k)
+                                for (int k = 0; k < 8; ++k)
 #pragma unroll
-                                for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
+                                    for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(o[4 * k + w]);
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                                    for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
+                            }
                         }
                         transpose8x8(a, p8);
                         const size_t col = (size_t)blk * 128 + (size_t)(64 * half + kSegCols * sg);
@@ -506,7 +543,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     constexpr bool F16 = decltype(fmt)::value;
                     const uint32_t ts = tmem + lrow + kTS + 32 * qq;
                     uint32_t pp[F16 ? 16 : 32];
-                    if (qq <= dq) {
+                    if (live(qq)) {
                         float x[32];
                         tmem_ld32(ts, x);
                         tmem_wait_ld();
@@ -527,10 +564,11 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     if (F16) tmem_st16(ts, pp);
                     else tmem_st32(ts, reinterpret_cast<const float*>(pp));
                 };
-                // V row kr of chunk c scaled in place by g^(B-1-kr), one key row per thread;
-                // fp16: also the fp16 copy Vz16.  The block lands after the previous P.Vz.
+                // V row kr of chunk c scaled in place by g^(B-1-kr) (reversed: g^kr), one key
+                // row per thread; fp16: also the fp16 copy Vz16.  The block lands after the
+                // previous P.Vz.
                 const int kr = 32 * (warp - kFirstP) + lane;
-                const float fz = exp2f(l2g * (float)(kB - 1 - kr));
+                const float fz = exp2f(l2g * (float)(rev ? kr : kB - 1 - kr));
                 float vmax = 0.f;
                 auto do_v = [&](int c) {
                     if (!wait(&bars.v_full, par(c))) return;
@@ -558,6 +596,12 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     arrive_lead(&bars.vz_ready);
                 };
                 for (int c = 0; c < nchunks && ok; ++c) {
+                    // the rows acc adds to this chunk's output, into L2 ahead of use
+                    if (ACC) {
+                        const float* ar = acc + (row_of(c) + j) * ldo + blk * 128 + 64 * half;
+                        prefetch_l2(ar);
+                        prefetch_l2(ar + 32);
+                    }
                     // V of this chunk (it lands while S runs), then P, then after P.Vz the output
                     do_v(c);
                     if (!wait(&bars.s_full, par(c))) break;
@@ -756,7 +800,7 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,
                                      cudaStream_t s, uint64_t wait_ns, int no_loads, int ldq,
-                                     int ldk, int ldv, int ldo) {
+                                     int ldk, int ldv, int ldo, int rev, const float* acc) {
     if (!chunkwise_pair_supported(dk, dv, chunk, hc, H)) return cudaErrorNotSupported;
     if (wait_ns == 0) wait_ns = kWaitLimitNs;
     if (ldq == 0) ldq = dk;
@@ -785,11 +829,14 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     const long long grid = 2LL * b * H * (dv / 128);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = kSmemBytes + 1024;
-    auto kern = out_bf16 ? chunkwise_pair_kernel<true> : chunkwise_pair_kernel<false>;
+    auto kern = acc ? (out_bf16 ? chunkwise_pair_kernel<true, true> : chunkwise_pair_kernel<false, true>)
+                    : (out_bf16 ? chunkwise_pair_kernel<true, false> : chunkwise_pair_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (acc && (reinterpret_cast<uintptr_t>(acc) & 15u)) return cudaErrorInvalidValue;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv,
-                                                fp16_first, dc, wait_ns, no_loads, ldo);
+                                                fp16_first, dc, wait_ns, no_loads, ldo, rev ? 1 : 0,
+                                                acc);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
     return e;

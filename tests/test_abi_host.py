@@ -289,6 +289,23 @@ def test_chunkwise_host_workspace_size(L):
     assert f(1, 0, -1, 2, 64, 64, 128) == 0
 
 
+def test_chunkwise_backward_workspace_size(L):
+    f = L.retention_chunkwise_backward_workspace_bytes
+    f.restype = ctypes.c_size_t
+    b, H, N, dk, dv = 2, 3, 512, 256, 512
+    st = b * H * dk * dv * 4                 # one fp32 state set: 6 MiB, 256-aligned
+    scales = 3 * 128 * 4                     # per-head scales, 1536 bytes (256-aligned)
+    # fp32 gradients: S0^T halves, dS^T halves, dS / g, the dv pass's final state, scales
+    assert f(0, b, H, N, dk, dv) == 4 * st + scales
+    # bf16 gradients add the fp32 partial sums of dq and dk over the halves
+    assert f(1, b, H, N, dk, dv) == 4 * st + scales + 2 * (b * H * N * dk * 4)
+    # one half (dv 256): no partial sums
+    assert f(1, b, H, N, dk, 256) == f(0, b, H, N, dk, 256)
+    assert f(0, b, H, N, 128, dv) == 0      # not a tensor-core shape
+    assert f(0, b, H, N, dk, 384) == 0
+    assert f(0, -1, H, N, dk, dv) == 0
+
+
 def test_chunkwise_host_rejections(L):
     before = binding.kernel_launches()
     assert hst(L, seg=96) == binding.RET_ERR_SHAPE                    # not a multiple of chunk
