@@ -88,6 +88,7 @@ cudaError_t launch_chunkwise_backward_simt(const void* q, const void* k, const v
                                            int dkk, int dvv, int chunk, const HeadConsts& hc,
                                            const float* state_in, const float* dstate_out,
                                            float* dstate_in, cudaStream_t s);
+unsigned read_clear_error_rglru(cudaStream_t s);
 cudaError_t launch_rglru_scan(const void* x, const void* ga, const void* gx, const float* lam,
                               const float* h0, void* y, float* h_last, int in_bf16, int out_bf16,
                               int b, int T, int D, float c, cudaStream_t s);

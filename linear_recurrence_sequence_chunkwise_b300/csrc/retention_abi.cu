@@ -400,7 +400,8 @@ int retention_check_device_error(void* stream) {
     cudaError_t ce = cudaStreamSynchronize(s);
     if (ce != cudaSuccess) return cuda_status(ce);
     unsigned e = ret::read_clear_error_tc_chunkwise(s) | ret::read_clear_error_tc_chunkwise_pair(s) |
-                 ret::read_clear_error_tc_parallel(s) | ret::read_clear_error_gemm(s);
+                 ret::read_clear_error_tc_parallel(s) | ret::read_clear_error_gemm(s) |
+                 ret::read_clear_error_rglru(s);
     ce = cudaGetLastError();
     if (ce != cudaSuccess) return cuda_status(ce);
     return e ? RET_ERR_TIMEOUT : RET_OK;

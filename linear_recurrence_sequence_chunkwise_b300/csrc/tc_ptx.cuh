@@ -116,11 +116,11 @@ __device__ __forceinline__ void bulk_wait_read0() {
 // Wait until the committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Hint: pull the box at (c0, c1) of a tiled tensor map into L2 (no completion signal).
-// the 128-byte line holding p into L2 (a hint: no fault on any address)
+// The 128-byte line holding p into L2 (a hint: no fault on any address).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
+// Hint: pull the box at (c0, c1) of a tiled tensor map into L2 (no completion signal).
 __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int c0, int c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),

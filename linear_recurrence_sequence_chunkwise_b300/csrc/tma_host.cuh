@@ -73,6 +73,23 @@ inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t planes
            CUDA_SUCCESS;
 }
 
+// Map over a bf16 tensor [planes][rows][cols] (cols * 2 bytes a multiple of 16), loading
+// boxes of 64 columns by box_rows rows of one plane with no swizzle (row r of the box at
+// byte r * 128).  Rows past `rows` in a plane read as zero.
+inline bool make_map_bf16_3d_plain(CUtensorMap* map, const void* base, uint64_t planes,
+                                   uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, rows, planes};
+    cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Map over a bf16 or fp32 tensor [planes][rows][cols] whose boxes are 128 bytes wide
 // (64 bf16 or 32 fp32 columns) by box_rows rows, 128-byte swizzle; used for the gate
 // tiles of the fused epilogue.

@@ -58,6 +58,29 @@ def test_bf16_parity_and_bf16_output():
     assert err_bf16_out(yb, want) <= 1.0
 
 
+@pytest.mark.parametrize("T", [1, 63, 65, 130])
+def test_bf16_states_gate_limits_and_ragged_tiles(T):
+    """bf16 inputs (the TMA-fed kernel, 64-step tiles): incoming and final states, T below,
+    just above and across tile boundaries, the recurrence gate closed on 8 channels, a = 0
+    and a = 1 on 8 channels each."""
+    b, D = 3, 128
+    x, ga, gx, lam, h0 = make(b, T, D, 500 + T, "bf16")
+    ga[:, :, :8] = -1e4
+    lam[8:16] = -1e4
+    lam[16:24] = 1e4
+    hl = torch.full((b, D), float("nan"), device=DEV)
+    y = rb.rglru_scan(x, ga, gx, lam, h0, 8.0, h_last=hl)
+    torch.cuda.synchronize()
+    assert rb.last_kernel() == "rglru"
+    want, want_h = oracle.rglru(x, ga, gx, lam, h0, 8.0, return_state=True)
+    assert err_bf16(y, want) < TOL_BF16
+    assert err_bf16(hl, want_h) < TOL_BF16
+    # r = 0 gives a_t = 1 and a zero input weight exactly: the state passes unchanged
+    assert torch.equal(y[:, :, :8], h0[:, None, :8].expand(b, T, 8))
+    assert torch.equal(hl[:, :8], h0[:, :8])
+    rb.check_device_error()
+
+
 def test_gate_limits_and_other_c():
     """Recurrence gate closed (r = 0: h stays h0), decay a = 0 (h = i x), a = 1, and
     c = 1 and 3.5 besides the page's 8."""
