@@ -7,12 +7,16 @@
 // for bf16 Q/K/V, fp32 accumulation and state, chunk B = 256, dk = 256, dv a multiple of
 // 128.
 //
-// Decay folding (no per-element power): V rows are scaled by zeta_r = g^(B-1-r) (Vz), the
-// scores by the constant a = g^(-B/2) with the causal mask (P = a S (.) M), the state copy
-// that Q multiplies by c = g^(B/2) (R' = c R), and each output row by xi_j = g^(j+1-B/2):
+// Decay folding (no per-element power): V rows are scaled by a zeta_r with zeta_r =
+// g^(B-1-r) and a constant a (Vz), the scores only masked (P = S (.) M), the state copy
+// that Q multiplies by c = a g^B (R' = c R), and each output row by xi_j = g^(j+1-B) / a:
 //     xi_j (P Vz + Q R')_j = sum_{r<=j} S_jr g^(j-r) v_r + g^(j+1) q_j R.
-// The state update is R <- g^B R (one TMEM pass per chunk), then R += K^T Vz.  Splitting
-// g^(-B) evenly between a and xi keeps both within g^(-B/2).
+// Tensor memory keeps R~ = a R, whose update R~ <- g^B R~ (one TMEM pass per chunk), then
+// R~ += K^T Vz, takes Vz as it is; the copy is R' = g^B R~, state_in enters times a and
+// state_out leaves times 1/a.  a is the power of two nearest g^(-B/2): splitting g^(-B)
+// evenly between Vz and xi keeps both within about g^(-B/2), and the state passes in and
+// out exactly.  In the reversed-time mode row r stands at position B-1-r (zeta_r = g^r,
+// xi_j = g^(-j) / a), the mask keeps keys r >= j and the chunks run from the last.
 //
 // Operand formats.  S = Q K^T and R += K^T Vz take bf16 operands as loaded (exact products).
 // The two products whose operands are computed take fp16 (11 significant bits, 8x finer
@@ -48,7 +52,7 @@
 //               TMEM lane quarter, one per 128-key half), then the chunk's output rows
 //               (one per 64-column half), coalesced stores
 //   warps 10-17 state copy (10-13 this CTA's own 64 value columns, 14-17 the peer's, into
-//               the peer's shared memory in 64-byte row pieces) with R <- g^B R, then
+//               the peer's shared memory in 64-byte row pieces) with R~ <- g^B R~, then
 //               Q -> fp16 in place (one row of one dk box per thread: dk 0-127 after S's
 //               first half, dk 128-255 after its second)
 // Warp w reaches TMEM lanes 32*(w%4)..+31.  Every wait is bounded; a wait that gives up
@@ -73,7 +77,7 @@
 //               boxes S no longer needs (the same offsets in both CTAs)
 //   V    32 KB  256 keys x own 64 value columns (scaled in place to bf16 Vz)
 //   V16  32 KB  fp16 Vz (hi/lo format: the lo part of R')
-//   R16  32 KB  fp16 R' = c R_{i-1}: 256 dk rows x own 64 columns (hi/lo format: hi part)
+//   R16  32 KB  fp16 R' = c R_{i-1} = g^B R~: 256 dk rows x own 64 columns (hi/lo: hi part)
 // MMA order in a chunk: S (dk boxes 0-1, then 2-3), Q.R' (dk 0-127, then 128-255), K^T.Vz
 // (key block 0, then 1), P.Vz.  Commits between the halves free shared memory early:
 // after S's first half the odd CTA loads its peer key block (boxes 0-1) and Q's first half
@@ -112,8 +116,10 @@ constexpr float kF16Max = 65504.0f;
 struct Decay {
     float l2g[kMaxHeads];   // log2(gamma)
     float gB[kMaxHeads];    // gamma^B
-    float a[kMaxHeads];     // gamma^(-B/2): score scale
-    float c[kMaxHeads];     // gamma^(B/2): state-copy scale
+    float l2a[kMaxHeads];   // log2 a: the integer nearest -B log2(gamma) / 2
+    float a[kMaxHeads];     // a = 2^l2a ~ gamma^(-B/2): score scale, carried by Vz and the
+                            // stored state (a power of two: state_in and state_out pass exactly)
+    float ia[kMaxHeads];    // 1 / a
 };
 
 struct Bars {
@@ -148,14 +154,15 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
 }
 
-template <bool OUT_BF16, bool ACC>
+template <bool OUT_BF16, bool ACC, bool REV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                       const __grid_constant__ CUtensorMap mv,
                       void* __restrict__ out_base, const float* __restrict__ state_in,
                       float* __restrict__ state_out, int N,
                       int H, int dv, int fp16_first, const Decay dc, uint64_t wait_ns,
-                      int no_loads, int ldo, int rev, const float* __restrict__ acc) {
+                      int no_loads, int ldo, const float* __restrict__ acc) {
+    constexpr bool rev = REV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = sm + kQOff;
@@ -435,20 +442,15 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
             if (warp < kFirstR) {
                 // ---------------------------------------------- scores -> P, then output
                 const int half = (warp - kFirstP) >> 2;  // key half (P) / 64-column half (O)
-                const float sa = dc.a[head];
-                // P = a S with the causal mask (key > j is zero; reversed: key < j).  Key
-                // quarter qq (32 keys) holds the diagonal of this warp's rows for qq = dq; the
+                // P = S with the causal mask (key > j is zero; reversed: key < j); the score
+                // scale a rides on Vz.  Key quarter qq (32 keys) holds the diagonal of this
+                // warp's rows for qq = dq (key 32 dq + e against row 32 dq + lane); the
                 // quarters on the far side of it are all zero (warp-uniform).
                 const int dq = 4 * (int)rank + q4;
-                float pmax = 0.f;
+                __half2 pmax2 = __float2half2_rn(0.f);   // largest |P| met (fp16 format)
                 auto live = [&](int qq) { return rev ? qq >= dq : qq <= dq; };
-                auto scaled = [&](const float* x, int qq, int e) {
-                    const int kc = 32 * qq + e;
-                    return (qq != dq || (rev ? kc >= j : kc <= j)) ? x[e] * sa : 0.f;
-                };
-                // xi_j = g^(j+1-B/2); reversed, row j stands at position B-1-j
-                const float xi = exp2f(l2g * (rev ? 0.5f * (float)kB - (float)j
-                                                  : (float)(j + 1) - 0.5f * (float)kB));
+                // xi_j = g^(j+1-B) / a; reversed, row j stands at position B-1-j: g^(-j) / a
+                const float xi = exp2f(l2g * (rev ? -(float)j : (float)(j + 1 - kB)) - dc.l2a[head]);
                 // output rows of chunk c: xi_j * O for this warp's 64 columns, straight from
                 // registers.  Each 128-byte row segment (32 fp32 or 64 bf16 columns = 8 items
                 // of 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so
@@ -547,14 +549,19 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                         float x[32];
                         tmem_ld32(ts, x);
                         tmem_wait_ld();
+                        if (qq == dq) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (rev ? e < lane : e > lane) x[e] = 0.f;
+                        }
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float y0 = scaled(x, qq, 2 * e), y1 = scaled(x, qq, 2 * e + 1);
                             if (F16) {
-                                pmax = fmaxf(pmax, fmaxf(fabsf(y0), fabsf(y1)));
-                                pp[e] = pack_f16(y0, y1);
+                                pp[e] = pack_f16(x[2 * e], x[2 * e + 1]);
+                                // fp16 rounds |x| >= 65520 to inf; NaN propagates
+                                pmax2 = __hmax2_nan(pmax2, __habs2(*reinterpret_cast<const __half2*>(&pp[e])));
                             } else {
-                                split2(y0, y1, pp[e], pp[(16 + e) % (F16 ? 16 : 32)]);
+                                split2(x[2 * e], x[2 * e + 1], pp[e], pp[(16 + e) % (F16 ? 16 : 32)]);
                             }
                         }
                     } else {
@@ -564,11 +571,11 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     if (F16) tmem_st16(ts, pp);
                     else tmem_st32(ts, reinterpret_cast<const float*>(pp));
                 };
-                // V row kr of chunk c scaled in place by g^(B-1-kr) (reversed: g^kr), one key
-                // row per thread; fp16: also the fp16 copy Vz16.  The block lands after the
-                // previous P.Vz.
+                // V row kr of chunk c scaled in place by a g^(B-1-kr) = g^(B/2-1-kr)
+                // (reversed: a g^kr), one key row per thread; fp16: also the fp16 copy Vz16.
+                // The block lands after the previous P.Vz.
                 const int kr = 32 * (warp - kFirstP) + lane;
-                const float fz = exp2f(l2g * (float)(rev ? kr : kB - 1 - kr));
+                const float fz = exp2f(l2g * (float)(rev ? kr : kB - 1 - kr) + dc.l2a[head]);
                 float vmax = 0.f;
                 auto do_v = [&](int c) {
                     if (!wait(&bars.v_full, par(c))) return;
@@ -616,13 +623,16 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                     arrive_lead(&bars.p_ready);
                     do_out(c);
                 }
-                if (f16) out_of_range(fmaxf(pmax, vmax));
+                if (f16)
+                    out_of_range(fmaxf(fmaxf(__low2float(pmax2), __high2float(pmax2)), vmax));
             } else {
                 // ---------------------------------------------- state copy; Q16 or V -> Vz
                 const int g = warp - kFirstR;            // 0..7
                 const bool remote = g >= 4;              // peer's 64 columns (else this CTA's own)
                 const uint32_t cbase = 64u * (remote ? peer : rank);   // TMEM column of the 64
-                const float gB = dc.gB[head], sc = dc.c[head];
+                // tensor memory holds the state scaled by a (R~ = a R: its update K^T Vz takes
+                // the a that Vz carries), so R' = c R = g^B R~; state_in enters times a
+                const float gB = dc.gB[head], sc = gB, sa = dc.a[head];
                 // fp16 R'16 (or the bf16 hi part) and, for hi/lo, the lo part
                 const uint32_t hi_peer = map_peer(sr16, peer);
                 const uint32_t lo_peer = map_peer(sv16, peer);
@@ -630,7 +640,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 const uint32_t j0 = (uint32_t)(j - p4);
                 float cmax = 0.f;
                 // State copy for chunk c: R' = c R_{i-1} (this CTA's dk row j, 64 value
-                // columns) into the B operand of Q.R', and R <- g^B R in TMEM, in two halves
+                // columns) into the B operand of Q.R', and R~ <- g^B R~ in TMEM, in two halves
                 // of 32 columns (4 items of 16 bytes per row).  Own columns go to this CTA's
                 // copy; the peer's columns are transposed within 4-lane groups so that each
                 // remote store writes 64 contiguous bytes of a row of the peer's copy.
@@ -646,7 +656,8 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const float4 f = src[e];
-                                x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
+                                x[4 * e] = sa * f.x; x[4 * e + 1] = sa * f.y;
+                                x[4 * e + 2] = sa * f.z; x[4 * e + 3] = sa * f.w;
                             }
                         } else {
 #pragma unroll
@@ -764,6 +775,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
         const uint32_t lrow = (uint32_t)(32 * q4) << 16;
         const int j = 128 * (int)rank + 32 * q4 + lane;
         const uint32_t cbase = 64u * ((warp - kFirstR >= 4) ? peer : rank);
+        const float sc = dc.ia[head];                // R = R~ / a
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
             float x[32];
@@ -773,7 +785,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 state_out + ((size_t)bh * kDk + j) * dv + blk * 128 + cbase + 32 * hh);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+                dst[e] = make_float4(sc * x[4 * e], sc * x[4 * e + 1], sc * x[4 * e + 2], sc * x[4 * e + 3]);
         }
     }
     tc_fence_before();
@@ -814,9 +826,11 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     for (int h = 0; h < H; ++h) {
         dc.l2g[h] = hc.l2g[h];
         dc.gB[h] = hc.gB[h];
-        dc.a[h] = exp2f(-0.5f * (float)chunk * hc.l2g[h]);
-        dc.c[h] = exp2f(0.5f * (float)chunk * hc.l2g[h]);
-        // fp16 Vz keeps ~11 bits down to g^(B-1) |v| only while g^(-B) <= 4096
+        dc.l2a[h] = rintf(-0.5f * (float)chunk * hc.l2g[h]);     // within [0, 32]
+        dc.a[h] = exp2f(dc.l2a[h]);
+        dc.ia[h] = exp2f(-dc.l2a[h]);
+        // fp16 Vz (a g^(B-1-r) v: between g^(B/2) |v| and g^(-B/2) |v|) keeps ~11 bits and
+        // stays in range only while g^(-B) <= 4096
         if (!(hc.l2g[h] * (float)chunk >= -12.0f)) fp16_first = 0;
     }
     const long long rows = (long long)b * H * N;
@@ -829,14 +843,18 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     const long long grid = 2LL * b * H * (dv / 128);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = kSmemBytes + 1024;
-    auto kern = acc ? (out_bf16 ? chunkwise_pair_kernel<true, true> : chunkwise_pair_kernel<false, true>)
-                    : (out_bf16 ? chunkwise_pair_kernel<true, false> : chunkwise_pair_kernel<false, false>);
+    decltype(&chunkwise_pair_kernel<false, false, false>) kern;
+    if (rev)
+        kern = acc ? (out_bf16 ? chunkwise_pair_kernel<true, true, true> : chunkwise_pair_kernel<false, true, true>)
+                   : (out_bf16 ? chunkwise_pair_kernel<true, false, true> : chunkwise_pair_kernel<false, false, true>);
+    else
+        kern = acc ? (out_bf16 ? chunkwise_pair_kernel<true, true, false> : chunkwise_pair_kernel<false, true, false>)
+                   : (out_bf16 ? chunkwise_pair_kernel<true, false, false> : chunkwise_pair_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (acc && (reinterpret_cast<uintptr_t>(acc) & 15u)) return cudaErrorInvalidValue;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv,
-                                                fp16_first, dc, wait_ns, no_loads, ldo, rev ? 1 : 0,
-                                                acc);
+                                                fp16_first, dc, wait_ns, no_loads, ldo, acc);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launch(RET_KERNEL_CHUNKWISE_TC_PAIR);
     return e;
