@@ -162,20 +162,23 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int ob = out_dtype == RET_BF16;
     if (in_dtype == RET_BF16) {
-        // The caller's chunk length first.  A chunk below 128 has no tensor-core schedule of
-        // its own; eq.(7) gives the same function for every chunk length (the chunk only
-        // orders the work: R_i carries everything before the chunk exactly), so such a call
-        // runs with 256-token chunks on the pair kernel, or 128-token chunks on the one-SM
-        // kernel, when N splits into them, and on the CUDA-core kernel otherwise.
-        const int schedule[3] = {chunk, 256, 128};
-        for (int i = 0; i < 3; ++i) {
+        // eq.(7) gives the same function for every chunk length (the chunk only orders the
+        // work: R_i carries everything before the chunk exactly), so the call runs on the
+        // fastest schedule that applies: the pair kernel with 256-token chunks when N splits
+        // into them, else the caller's chunk length (pair kernel, then one-SM kernel); a
+        // chunk below 128 has no tensor-core schedule of its own and runs with 256- or
+        // 128-token chunks when N splits into them, on the CUDA-core kernel otherwise.
+        const int schedule[4] = {256, chunk, 256, 128};
+        for (int i = 0; i < 4; ++i) {
             const int cb = schedule[i];
-            if (i > 0 && (chunk >= 128 || N % cb != 0)) continue;
+            if (N % cb != 0 || (i == 0 && cb == chunk)) continue;
+            if (i >= 2 && chunk >= 128) continue;
             HeadConsts hcb;
             if (head_consts(gamma, H, cb, &hcb) != RET_OK) continue;
             cudaError_t e = ret::launch_chunkwise_tc_pair(q, k, v, o, ob, b, H, N, dk, dv, cb,
                                                           hcb, state_in, state_out, s);
             if (e != cudaErrorNotSupported) return cuda_status(e);
+            if (i == 0) continue;          // the first entry is for the pair kernel only
             e = ret::launch_chunkwise_tc(q, k, v, o, ob, b, H, N, dk, dv, cb, hcb, state_in,
                                          state_out, s);
             if (e != cudaErrorNotSupported) return cuda_status(e);

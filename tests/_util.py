@@ -43,10 +43,13 @@ def err_bf16_out(got, want):
     return float(np.max(np.abs(g - w) / (TOL_BF16 * rms + 2.0 ** -8 * np.abs(w))))
 
 
-def chunkwise_tc_name(dk, dv, chunk):
-    """Tensor-core chunkwise kernel the library picks for bf16 inputs of this shape:
-    the pair-of-SMs kernel for chunk 256, dk 256, dv a multiple of 128."""
-    return "chunkwise_tc_pair" if (chunk == 256 and dk == 256 and dv % 128 == 0) else "chunkwise_tc"
+def chunkwise_tc_name(dk, dv, chunk, N):
+    """Tensor-core chunkwise kernel the library picks for bf16 inputs of this shape (decays
+    within the pair kernel's range): the pair-of-SMs kernel, with 256-token chunks, for
+    dk 256 and dv a multiple of 128 when N is a multiple of 256 (the function does not
+    depend on the chunk length); the one-SM kernel otherwise."""
+    pair = dk == 256 and dv % 128 == 0 and (chunk == 256 or N % 256 == 0)
+    return "chunkwise_tc_pair" if pair else "chunkwise_tc"
 
 
 def guarded(shape, dtype, device, pad=64):

@@ -56,8 +56,8 @@ def test_sweep_point(N, chunk):
     q, k, v = inputs.qkv(w, DEV)
     out = rb.retention_chunkwise(q, k, v, w.gamma, w.chunk, out_dtype=torch.bfloat16)
     rb.check_device_error()
-    # every point on tensor cores: chunk 64 runs with the 256-token schedule (same function)
-    assert rb.last_kernel() == ("chunkwise_tc" if chunk == 128 else "chunkwise_tc_pair")
+    # every point on tensor cores, with the 256-token schedule (the same function)
+    assert rb.last_kernel() == "chunkwise_tc_pair"
     idx = [(3, 0), (1, 9)]
     us = units_of(q, k, v, idx)
     outs = oracle.map_units(lambda u: oracle.chunkwise(u[2], u[3], u[4], [w.gamma[u[1]]], w.chunk),

@@ -43,7 +43,7 @@ def test_streamed_equals_single_call(dk, dv, chunk, seg):
     ho.fill_(float("nan"))
     rb.retention_chunkwise_host(hq, hk, hv, g, chunk, ho, seg)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk, seg)
     one = rb.retention_chunkwise(hq.to(DEV), hk.to(DEV), hv.to(DEV), g, chunk).cpu()
     assert not torch.isnan(ho).any()
     assert err_f32(ho, one) < 1e-5

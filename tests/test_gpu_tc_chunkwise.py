@@ -40,8 +40,25 @@ def test_tc_chunkwise_shapes(chunk, dk, dv):
     q, k, v = mk(b, H, N, dk, dv, 100 + dk + dv)
     g = [0.96875, 0.9990234375]
     got = rb.retention_chunkwise(q, k, v, g, chunk)
-    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk, N)
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
+    rb.check_device_error()
+
+
+@pytest.mark.parametrize("dv", [128, 512])
+def test_one_sm_kernel_at_dk256_when_n_has_no_256_split(dv):
+    """chunk 128 with N = 384 (no 256-token split): the one-SM tensor-core kernel, dk 256,
+    with incoming and final states."""
+    b, H, N, dk = 2, 2, 384, 256
+    q, k, v = mk(b, H, N, dk, dv, 150 + dv)
+    g = [0.96875, 0.9990234375]
+    s0 = inputs.randn((b, H, dk, dv), 151, 0.05, "f32", DEV)
+    so = torch.empty_like(s0)
+    got = rb.retention_chunkwise(q, k, v, g, 128, state_in=s0, state_out=so)
+    assert rb.last_kernel() == "chunkwise_tc"
+    want, s_end = oracle.chunkwise(q, k, v, g, 128, state_in=s0, return_state=True)
+    assert err_bf16(got, want) < TOL_BF16
+    assert err_f32(so, s_end) < TOL_BF16
     rb.check_device_error()
 
 
@@ -52,7 +69,7 @@ def test_tc_chunkwise_decay_range(chunk):
     q, k, v = mk(b, H, N, dk, dv, 200)
     g = [0.71 if chunk == 128 else 0.845, 0.9, 0.999, 1.0 - 2.0 ** -20]
     got = rb.retention_chunkwise(q, k, v, g, chunk)
-    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk, N)
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
 
 
@@ -93,7 +110,7 @@ def test_tc_chunkwise_states_and_bf16_out(chunk):
                                             v[:, :, sl].contiguous(), g, chunk,
                                             state_in=st if lo else None, state_out=st,
                                             out_dtype=torch.bfloat16))
-        assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
+        assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk, half)
     assert err_bf16_out(torch.cat(parts, dim=2), want) < 1.0
     assert err_f32(st, s_end) < TOL_BF16
 
@@ -133,7 +150,7 @@ def test_tc_chunkwise_repeatable_and_guarded(chunk, dv):
     first = o.clone()
     rb.retention_chunkwise(q, k, v, g, chunk, out=o)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk)
+    assert rb.last_kernel() == chunkwise_tc_name(dk, dv, chunk, N)
     assert torch.equal(first, o)
     assert guards_intact(buf)
     assert err_bf16(o, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
