@@ -157,20 +157,22 @@ class Clocks:
                 "samples": len(rows), "samples_under_load": len(busy), "reasons": reasons}
 
 
-def profile_traffic(summary_name: str, source_file: str):
-    """DRAM bytes per launch from a committed ncu summary, or None when the kernel
-    source changed since the counters were taken (the summary records its hash)."""
+def profile_traffic(summary_name: str, *source_files: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when a kernel source
+    changed since the counters were taken (the summary records the hash of each source)."""
     path = os.path.join(ROOT, "profiles", summary_name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    hashes = set(re.findall(r"source_sha256:\s*([0-9a-f]{64})", text))
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_hash and m_bytes):
+    if not (hashes and m_bytes):
         return None
-    src = os.path.join(ROOT, "linear_recurrence_sequence_chunkwise_b300", "csrc", source_file)
-    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m_bytes.group(1)) if cur == m_hash.group(1) else None
+    for f in source_files:
+        src = os.path.join(ROOT, "linear_recurrence_sequence_chunkwise_b300", "csrc", f)
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() not in hashes:
+            return None
+    return float(m_bytes.group(1))
 
 
 def timed(fn, steps: int, warmup: int, dist: Dist, stream=None, counter=None):
@@ -437,7 +439,7 @@ def bench_backward(args, dist, rb, pk):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                          "traffic": profile_traffic("chunkwise_backward_tc_backward.md",
-                                                    "backward_tc.cu"),
+                                                    "backward_tc.cu", "tc_chunkwise_pair.cu"),
                          "algorithmic_flops_per_launch": flops},
             "cuda_core_kernel_ms_per_step": ms_cc / 3}
 
@@ -613,7 +615,8 @@ def bench_gemm(args, dist, rb, pk):
                         "accumulate, bf16 out (retention_gemm)",
             "value": value, "unit": "rows/s", "ms_per_step": ms_step,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "traffic": profile_traffic("gemm_kernel_gemm.md", "tc_gemm.cu"),
                          "algorithmic_flops_per_launch": flops}}
 
 
