@@ -20,8 +20,10 @@
 //               a time: optional rotation, then coalesced stores (8-lane transposes: every
 //               store instruction writes four whole 128-byte segments)
 // The two accumulators let the epilogue of one tile overlap the MMAs of the next.  Tiles
-// are 128 rows x 256 columns, walked with the column index fastest so that the CTAs
-// running at one time share their A rows and weight columns in L2.  Every wait is bounded
+// are 128 rows x 256 columns, walked in bands of 16 row tiles, the row index fastest inside
+// a band: the ~148 tiles in flight at one time then cover about 16 row panels of A and 9
+// column panels of W (~35 MB at K = 4096), which stay in L2 while they are reused, instead
+// of all of W (the row-major order's working set).  Every wait is bounded
 // (2 s); a wait that gives up sets the device error word and the CTA unwinds.
 //
 // xPos phase: p * theta_j / (2 pi) turns, reduced exactly as 64-bit fixed point:
@@ -60,6 +62,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
+constexpr int kBand = 16;          // row tiles per band of the tile order
+
+// Tile t of the order above -> its first row and column.
+__device__ __forceinline__ void tile_origin(int t, int mtiles, int ntiles, int& m0, int& n0) {
+    const int band = t / (kBand * ntiles);
+    const int first = band * kBand;
+    const int rows = min(kBand, mtiles - first);
+    const int r = t - band * kBand * ntiles;
+    m0 = (first + r % rows) * kTileM;
+    n0 = (r / rows) * kTileN;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mw,
             int M, int Nc, int K, const __grid_constant__ GemmEpilogue ep) {
@@ -96,7 +110,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUte
             uint32_t issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                const int m0 = (t / ntiles) * kTileM, n0 = (t % ntiles) * kTileN;
+                int m0, n0;
+                tile_origin(t, mtiles, ntiles, m0, n0);
                 for (int ks = 0; ks < ksteps; ++ks, ++it) {
                     const uint32_t s = it % kStages, use = it / kStages;
                     if (use > 0 && !mbar_wait(&bars.empty[s], (use - 1) & 1, abort_p)) {
@@ -162,7 +177,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUte
         uint32_t tl = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tl) {
-            const int m0 = (t / ntiles) * kTileM, n0 = (t % ntiles) * kTileN;
+            int m0, n0;
+            tile_origin(t, mtiles, ntiles, m0, n0);
             const uint32_t buf = tl & 1, use = tl >> 1;
             const bool got = __all_sync(0xffffffffu, mbar_wait(&bars.acc_full[buf], use & 1, abort_p));
             if (!got) { ok = false; if (lane == 0) fail(); break; }
