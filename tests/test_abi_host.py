@@ -289,6 +289,31 @@ def test_chunkwise_host_workspace_size(L):
     assert f(1, 0, -1, 2, 64, 64, 128) == 0
 
 
+def test_chunkwise_backward_ws_rejections(L):
+    """The tensor-core shape (bf16, dk 256, dv 512, N 512): a missing, misaligned or short
+    workspace is refused before any launch; other shapes keep the CUDA-core checks."""
+    W256 = ctypes.c_void_p(0x300000)          # 256-byte aligned, never dereferenced
+    W16 = ctypes.c_void_p(0x300010)           # 16-byte but not 256-byte aligned
+    need = L.retention_chunkwise_backward_workspace_bytes(0, 1, 2, 512, 256, 512)
+    assert need > 0
+
+    def ws(w=W256, nbytes=None, dk=256, dv=512, N=512, it=1, gq=A2):
+        return L.retention_chunkwise_backward_ws(A, A, A, A, gq, A2, A2, it, 0, 1, 2, N, dk, dv,
+                                                 256 if N % 256 == 0 else 64, G(0.97, 0.99),
+                                                 None, None, None, w,
+                                                 ctypes.c_size_t(need if nbytes is None else nbytes), S)
+
+    before = binding.kernel_launches()
+    assert ws(w=NUL) == binding.RET_ERR_NULL
+    assert ws(w=W16) == binding.RET_ERR_ALIGN
+    assert ws(nbytes=need - 1) == binding.RET_ERR_SHAPE
+    assert ws(gq=MIS) == binding.RET_ERR_ALIGN
+    assert ws(gq=NUL) == binding.RET_ERR_NULL
+    assert ws(dk=24, w=NUL) == binding.RET_ERR_UNSUPPORTED     # CUDA-core checks, no workspace
+    assert ws(it=5) == binding.RET_ERR_DTYPE
+    assert binding.kernel_launches() == before
+
+
 def test_chunkwise_backward_workspace_size(L):
     f = L.retention_chunkwise_backward_workspace_bytes
     f.restype = ctypes.c_size_t
