@@ -399,7 +399,8 @@ def bench_parallel(args, dist, rb, pk):
             "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                         "traffic": profile_traffic(f"parallel_tc_{w.name}.md", "tc_parallel.cu"),
+                         "traffic": profile_traffic(f"parallel_pair_{w.name}.md", "tc_parallel_pair.cu",
+                                                    "tc_parallel.cu"),
                          "algorithmic_flops_per_launch": flops}}
 
 

@@ -393,6 +393,15 @@ int retention_project_heads(const void* x, const void* w, void* out, int b, int 
 int retention_chunkwise_format_reruns(void* stream);
 
 /*
+ * The same diagnostic for the parallel form on pairs of SMs (dk 256, dv and N multiples of
+ * 256): P and V enter the score x value product as fp16; a unit whose P or V leaves fp16's
+ * range, or whose largest |v| is below 2^-6 (typical values then near fp16's subnormals),
+ * is recomputed with hi/lo bf16 P inside the same launch.  Counts clusters (the value-column
+ * blocks of a query block with the fused epilogue, else one SM pair) that re-ran.
+ */
+int retention_parallel_format_reruns(void* stream);
+
+/*
  * Self-test of the bounded on-chip waits (the pages describe no fault handling; this is the
  * library's own).  Launches the pair-of-SMs chunkwise kernel on b1 H1 N256 dk256 dv128
  * (q, k: 256 x 256 bf16, v: 256 x 128 bf16, o: 256 x 128 fp32, DEVICE buffers that are
@@ -437,7 +446,9 @@ enum {
     RET_KERNEL_RGLRU = 10,          /* RG-LRU scan                                    */
     RET_KERNEL_XPOS = 11,           /* xPos rotation of Q and K                       */
     RET_KERNEL_GEMM_TC = 12,        /* projection GEMM of the layer, tensor cores     */
-    RET_KERNEL_CHUNKWISE_BACKWARD_TC = 13 /* chunkwise gradient as pair-kernel passes   */
+    RET_KERNEL_CHUNKWISE_BACKWARD_TC = 13, /* chunkwise gradient as pair-kernel passes  */
+    RET_KERNEL_PARALLEL_TC_PAIR = 14, /* parallel form, tensor cores on pairs of SMs      */
+    RET_KERNEL_PARALLEL_GATED_TC_PAIR = 15 /* parallel form + gated GroupNorm, SM pairs  */
 };
 
 /*

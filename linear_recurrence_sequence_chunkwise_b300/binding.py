@@ -26,7 +26,7 @@ NORM_ALL = 7
 KERNEL_NAMES = {0: "none", 1: "parallel_simt", 2: "chunkwise_simt", 3: "decode", 4: "epilogue",
                 5: "chunkwise_tc", 6: "parallel_tc", 7: "parallel_gated_tc", 8: "chunkwise_tc_pair",
                 9: "chunkwise_backward_simt", 10: "rglru", 11: "xpos", 12: "gemm_tc",
-                13: "chunkwise_backward_tc"}
+                13: "chunkwise_backward_tc", 14: "parallel_tc_pair", 15: "parallel_gated_tc_pair"}
 
 _lib = None
 _lock = threading.Lock()
@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
             L.retention_chunkwise_wait_selftest.restype = ctypes.c_int
             L.retention_chunkwise_format_reruns.argtypes = [vp]
             L.retention_chunkwise_format_reruns.restype = ctypes.c_int
+            L.retention_parallel_format_reruns.argtypes = [vp]
+            L.retention_parallel_format_reruns.restype = ctypes.c_int
             L.retention_kernel_launches.argtypes = []
             L.retention_kernel_launches.restype = ctypes.c_ulonglong
             L.retention_last_kernel.argtypes = []
@@ -518,6 +520,15 @@ def chunkwise_format_reruns(stream=None) -> int:
     n = int(lib().retention_chunkwise_format_reruns(_stream(stream)))
     if n < 0:
         raise RetentionError("retention_chunkwise_format_reruns", RET_ERR_CUDA, "sync failed")
+    return n
+
+
+def parallel_format_reruns(stream=None) -> int:
+    """Synchronise and return (and reset) how many clusters of the pair-of-SMs parallel kernel
+    re-ran in the bf16 hi/lo format (fp16 range left, or V too small for fp16)."""
+    n = int(lib().retention_parallel_format_reruns(_stream(stream)))
+    if n < 0:
+        raise RetentionError("retention_parallel_format_reruns", RET_ERR_CUDA, "sync failed")
     return n
 
 

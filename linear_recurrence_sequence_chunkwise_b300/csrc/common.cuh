@@ -123,6 +123,16 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
                                      int dk, int dv, const HeadConsts& hc, unsigned flags,
                                      float eps, const float* weight, const float* bias,
                                      cudaStream_t s);
+// Parallel form on pairs of SMs (tc_parallel_pair.cu): bf16 inputs, dk 256, dv a multiple
+// of 256, N a multiple of 256; epi 0 plain output ([b][H][N][dv]), 1 / 2 the gated
+// GroupNorm epilogue with an fp32 / bf16 gate ([b][N][H*dv]).  cudaErrorNotSupported
+// for other shapes.
+cudaError_t launch_parallel_pair(const void* q, const void* k, const void* v, const void* g,
+                                 void* out, int out_bf16, int epi, int b, int H, int N, int dk,
+                                 int dv, const HeadConsts& hc, unsigned flags, float eps,
+                                 const float* weight, const float* bias, cudaStream_t s);
+unsigned read_clear_error_parallel_pair(cudaStream_t s);
+unsigned read_clear_reruns_parallel_pair(cudaStream_t s);
 // Gradient of the chunkwise form as pair-kernel passes (backward_tc.cu): bf16 inputs,
 // dk 256, dv a multiple of 256, N a multiple of 256, decays the pair kernel takes at chunk
 // 256 (hc256: head constants for chunk 256).  workspace: chunkwise_backward_tc_workspace

@@ -398,13 +398,19 @@ int retention_chunkwise_format_reruns(void* stream) {
     return (int)ret::read_clear_reruns_tc_chunkwise_pair(s);
 }
 
+int retention_parallel_format_reruns(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+    return (int)ret::read_clear_reruns_parallel_pair(s);
+}
+
 int retention_check_device_error(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce = cudaStreamSynchronize(s);
     if (ce != cudaSuccess) return cuda_status(ce);
     unsigned e = ret::read_clear_error_tc_chunkwise(s) | ret::read_clear_error_tc_chunkwise_pair(s) |
                  ret::read_clear_error_tc_parallel(s) | ret::read_clear_error_gemm(s) |
-                 ret::read_clear_error_rglru(s);
+                 ret::read_clear_error_rglru(s) | ret::read_clear_error_parallel_pair(s);
     ce = cudaGetLastError();
     if (ce != cudaSuccess) return cuda_status(ce);
     return e ? RET_ERR_TIMEOUT : RET_OK;

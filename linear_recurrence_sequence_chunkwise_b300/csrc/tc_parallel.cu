@@ -648,6 +648,10 @@ cudaError_t launch_common(const void* q, const void* k, const void* v, void* o, 
 cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, void* o, int out_bf16,
                                int b, int H, int N, int dk, int dv, const HeadConsts& hc,
                                unsigned flags, cudaStream_t s) {
+    // pairs of SMs where the shape allows (dk 256, dv and N multiples of 256)
+    const cudaError_t ep = launch_parallel_pair(q, k, v, nullptr, o, out_bf16, 0, b, H, N, dk, dv,
+                                                hc, flags, 0.f, nullptr, nullptr, s);
+    if (ep != cudaErrorNotSupported) return ep;
     EpiArgs ea{};
     ea.out = o;
     return launch_common(q, k, v, o, out_bf16, b, H, N, dk, dv, hc, flags, 0, ea, s);
@@ -658,6 +662,9 @@ cudaError_t launch_parallel_gated_tc(const void* q, const void* k, const void* v
                                      int dk, int dv, const HeadConsts& hc, unsigned flags,
                                      float eps, const float* weight, const float* bias,
                                      cudaStream_t s) {
+    const cudaError_t ep = launch_parallel_pair(q, k, v, g, out, out_bf16, g_bf16 ? 2 : 1, b, H, N,
+                                                dk, dv, hc, flags, eps, weight, bias, s);
+    if (ep != cudaErrorNotSupported) return ep;
     EpiArgs ea;
     ea.out = out;
     ea.g = g;

@@ -52,6 +52,14 @@ def chunkwise_tc_name(dk, dv, chunk, N):
     return "chunkwise_tc_pair" if pair else "chunkwise_tc"
 
 
+def parallel_tc_name(dk, dv, N, gated=False):
+    """Tensor-core parallel kernel the library picks for bf16 inputs of this shape: the
+    pair-of-SMs kernel for dk 256 with dv and N multiples of 256, the one-SM kernel for
+    the other tensor-core shapes."""
+    pair = dk == 256 and dv % 256 == 0 and N % 256 == 0 and N >= 256
+    return ("parallel_gated_tc" if gated else "parallel_tc") + ("_pair" if pair else "")
+
+
 def guarded(shape, dtype, device, pad=64):
     """A tensor view with `pad` sentinel elements on each side (canary guard bands)."""
     n = int(np.prod(shape))

@@ -40,6 +40,7 @@ def test_exports_every_declared_function(L):
                           "retention_chunkwise_host_static_scratch_bytes",
                           "retention_chunkwise_backward", "rglru_scan",
                           "retention_xpos_rotate", "retention_chunkwise_format_reruns",
+                          "retention_parallel_format_reruns",
                           "retention_chunkwise_wait_selftest", "retention_msr_layer",
                           "retention_msr_layer_workspace_bytes", "retention_gemm",
                           "retention_project_heads", "retention_chunkwise_backward_ws",

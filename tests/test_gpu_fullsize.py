@@ -94,7 +94,7 @@ def test_parallel_norm_full_fused_gated():
     q, k, v = inputs.qkv(w, DEV)
     g = inputs.gate(w, DEV)
     out = rb.retention_parallel_gated(q, k, v, g, w.gamma, w.flags, w.eps)
-    assert rb.last_kernel() == "parallel_gated_tc"
+    assert rb.last_kernel() == "parallel_gated_tc_pair"
     rb.check_device_error()
     idx = [(0, 0), (7, 7), (5, 2)]
     us = units_of(q, k, v, idx)

@@ -13,7 +13,7 @@ import oracle
 from linear_recurrence_sequence_chunkwise_b300 import binding as rb
 from linear_recurrence_sequence_chunkwise_b300 import inputs
 
-from _util import TOL_BF16, err_bf16, err_bf16_out, guarded, guards_intact
+from _util import TOL_BF16, err_bf16, err_bf16_out, guarded, guards_intact, parallel_tc_name
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -35,25 +35,27 @@ def mk(b, H, N, dk, dv, seed, std=1.0):
 
 @pytest.mark.parametrize("flags", [0, 1, 2, 4, 7])
 @pytest.mark.parametrize("dk,dv", [(256, 512), (128, 128), (256, 384), (128, 256)])
-def test_tc_parallel_shapes_and_flags(dk, dv, flags):
-    b, H, N = 1, 2, 384
-    q, k, v = mk(b, H, N, dk, dv, 1000 + dk + dv + flags)
+@pytest.mark.parametrize("N", [384, 512])
+def test_tc_parallel_shapes_and_flags(dk, dv, flags, N):
+    """N = 512 with dk 256 and dv 512 runs on pairs of SMs; the rest on one SM."""
+    b, H = 1, 2
+    q, k, v = mk(b, H, N, dk, dv, 1000 + dk + dv + flags + N)
     g = [0.96875, 0.9990234375]
     got = rb.retention_parallel(q, k, v, g, flags)
-    assert rb.last_kernel() == "parallel_tc"
+    assert rb.last_kernel() == parallel_tc_name(dk, dv, N)
     assert err_bf16(got, oracle.parallel(q, k, v, g, flags)) < TOL_BF16
     rb.check_device_error()
 
 
-@pytest.mark.parametrize("N", [1, 77, 128, 129, 200, 520])
+@pytest.mark.parametrize("N", [1, 77, 128, 129, 200, 256, 520, 768])
 def test_tc_parallel_ragged_sequence(N):
     """N not a multiple of the 128-row tile: the partial tiles are masked (N < 128
-    goes to the CUDA-core kernel)."""
+    goes to the CUDA-core kernel); multiples of 256 run on pairs of SMs."""
     b, H, dk, dv = 2, 2, 256, 256
     q, k, v = mk(b, H, N, dk, dv, 2000 + N)
     g = [0.9, 0.99]
     got = rb.retention_parallel(q, k, v, g, 7)
-    assert rb.last_kernel() == ("parallel_tc" if N >= 128 else "parallel_simt")
+    assert rb.last_kernel() == (parallel_tc_name(dk, dv, N) if N >= 128 else "parallel_simt")
     assert err_bf16(got, oracle.parallel(q, k, v, g, 7)) < TOL_BF16
 
 
@@ -68,16 +70,17 @@ def test_tc_parallel_special_decays():
         assert err_bf16(got, oracle.parallel(q, k, v, g, flags)) < TOL_BF16, flags
 
 
-def test_tc_parallel_bf16_output_guarded_and_repeatable():
-    b, H, N, dk, dv = 2, 3, 260, 256, 512
-    q, k, v = mk(b, H, N, dk, dv, 4000)
+@pytest.mark.parametrize("N", [260, 512])
+def test_tc_parallel_bf16_output_guarded_and_repeatable(N):
+    b, H, dk, dv = 2, 3, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 4000 + N)
     g = inputs.gammas(H)
     buf, o = guarded((b, H, N, dv), torch.bfloat16, DEV)
     rb.retention_parallel(q, k, v, g, 7, out=o)
     first = o.clone()
     rb.retention_parallel(q, k, v, g, 7, out=o)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == "parallel_tc"
+    assert rb.last_kernel() == parallel_tc_name(dk, dv, N)
     assert torch.equal(first, o)
     assert guards_intact(buf)
     assert err_bf16_out(o, oracle.parallel(q, k, v, g, 7)) < 1.0
@@ -99,7 +102,7 @@ def test_tc_parallel_matches_cuda_core_kernel_on_fp32_copy():
 
 # ---------------------------------------------------------------- fused gated epilogue
 @pytest.mark.parametrize("dk,dv,N", [(256, 512, 256), (128, 256, 200), (256, 384, 384),
-                                     (128, 128, 130)])
+                                     (128, 128, 130), (256, 256, 512), (256, 512, 768)])
 @pytest.mark.parametrize("flags", [0, 7])
 def test_tc_parallel_gated_matches_oracle(dk, dv, N, flags):
     """GroupNorm over each (token, head) spans the value-column blocks of a cluster."""
@@ -108,16 +111,18 @@ def test_tc_parallel_gated_matches_oracle(dk, dv, N, flags):
     gate = inputs.randn((b, N, H * dv), 6100 + N, 1.0, "bf16", DEV)
     g = [0.96875, 0.999]
     got = rb.retention_parallel_gated(q, k, v, gate, g, flags, 1e-5)
-    assert rb.last_kernel() == "parallel_gated_tc"
+    assert rb.last_kernel() == parallel_tc_name(dk, dv, N, gated=True)
     want = oracle.msr_epilogue(oracle.parallel(q, k, v, g, flags), gate, 1e-5)
     assert err_bf16(got, want) < TOL_BF16
     rb.check_device_error()
 
 
 @pytest.mark.parametrize("g_dtype,out_dtype", [(torch.float32, torch.float32),
-                                               (torch.bfloat16, torch.bfloat16)])
-def test_tc_parallel_gated_affine_dtypes_guarded(g_dtype, out_dtype):
-    b, H, N, dk, dv = 1, 3, 260, 256, 512
+                                               (torch.bfloat16, torch.bfloat16),
+                                               (torch.float32, torch.bfloat16)])
+@pytest.mark.parametrize("N", [260, 512])
+def test_tc_parallel_gated_affine_dtypes_guarded(g_dtype, out_dtype, N):
+    b, H, dk, dv = 1, 3, 256, 512
     q, k, v = mk(b, H, N, dk, dv, 6500)
     gate = inputs.randn((b, N, H * dv), 6501, 1.0, "f32", DEV).to(g_dtype)
     w = inputs.randn((H * dv,), 6502, 1.0, "f32", DEV)
@@ -126,7 +131,7 @@ def test_tc_parallel_gated_affine_dtypes_guarded(g_dtype, out_dtype):
     buf, out = guarded((b, N, H * dv), out_dtype, DEV)
     rb.retention_parallel_gated(q, k, v, gate, g, 7, 1e-5, w, bias, out=out)
     torch.cuda.synchronize()
-    assert rb.last_kernel() == "parallel_gated_tc"
+    assert rb.last_kernel() == parallel_tc_name(dk, dv, N, gated=True)
     assert guards_intact(buf)
     want = oracle.msr_epilogue(oracle.parallel(q, k, v, g, 7), gate, 1e-5, w, bias)
     if out_dtype == torch.bfloat16:
@@ -135,11 +140,12 @@ def test_tc_parallel_gated_affine_dtypes_guarded(g_dtype, out_dtype):
         assert err_bf16(out, want) < TOL_BF16
 
 
-def test_tc_parallel_gated_equals_two_call_path():
+@pytest.mark.parametrize("N", [384, 512])
+def test_tc_parallel_gated_equals_two_call_path(N):
     """One pass equals retention_parallel followed by msr_epilogue on the GPU."""
-    b, H, N, dk, dv = 2, 2, 384, 256, 512
-    q, k, v = mk(b, H, N, dk, dv, 6600)
-    gate = inputs.randn((b, N, H * dv), 6601, 1.0, "bf16", DEV)
+    b, H, dk, dv = 2, 2, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 6600 + N)
+    gate = inputs.randn((b, N, H * dv), 6601 + N, 1.0, "bf16", DEV)
     g = [0.9, 0.995]
     fused = rb.retention_parallel_gated(q, k, v, gate, g, 7, 1e-5)
     two = rb.msr_epilogue(rb.retention_parallel(q, k, v, g, 7), gate, 1e-5)
@@ -152,3 +158,55 @@ def test_tc_parallel_gated_unsupported_shape_is_rejected():
     with pytest.raises(rb.RetentionError) as ei:
         rb.retention_parallel_gated(q, k, v, gate, [0.9], 7)
     assert ei.value.status == rb.RET_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- pairs of SMs: fp16 format
+@pytest.mark.parametrize("gated", [False, True])
+def test_pair_fp16_no_rerun_at_unit_scale(gated):
+    """N(0,1) inputs: P and V stay inside fp16's range, no unit re-runs."""
+    b, H, N, dk, dv = 1, 2, 512, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 7000)
+    g = [0.96875, 0.999]
+    rb.parallel_format_reruns()
+    if gated:
+        gate = inputs.randn((b, N, H * dv), 7001, 1.0, "bf16", DEV)
+        got = rb.retention_parallel_gated(q, k, v, gate, g, 7, 1e-5)
+        want = oracle.msr_epilogue(oracle.parallel(q, k, v, g, 7), gate, 1e-5)
+    else:
+        got = rb.retention_parallel(q, k, v, g, 7)
+        want = oracle.parallel(q, k, v, g, 7)
+    assert rb.last_kernel() == parallel_tc_name(dk, dv, N, gated)
+    assert rb.parallel_format_reruns() == 0
+    assert err_bf16(got, want) < TOL_BF16
+    rb.check_device_error()
+
+
+@pytest.mark.parametrize("what", ["scores_beyond_fp16", "v_beyond_fp16", "v_below_fp16"])
+@pytest.mark.parametrize("gated", [False, True])
+def test_pair_reruns_units_outside_fp16(what, gated):
+    """A head whose scores (|P| > 65504), V (|v| > 65504) or V scale (max |v| < 2^-6) does not
+    suit fp16 is recomputed with hi/lo bf16 P inside the launch; the result still matches."""
+    b, H, N, dk, dv = 1, 2, 512, 256, 512
+    q, k, v = mk(b, H, N, dk, dv, 7100)
+    if what == "scores_beyond_fp16":
+        q[:, 1] *= 64.0
+        k[:, 1] *= 64.0            # |q.k| up to ~1e5 (flags 0: no score scale)
+    elif what == "v_beyond_fp16":
+        v[:, 1] *= 2.0 ** 17
+    else:
+        v[:, 1] *= 2.0 ** -12
+    g = [0.96875, 0.999]
+    rb.parallel_format_reruns()
+    if gated:
+        gate = inputs.randn((b, N, H * dv), 7101, 1.0, "bf16", DEV)
+        got = rb.retention_parallel_gated(q, k, v, gate, g, 0, 1e-5)
+        want = oracle.msr_epilogue(oracle.parallel(q, k, v, g, 0), gate, 1e-5)
+    else:
+        got = rb.retention_parallel(q, k, v, g, 0)
+        want = oracle.parallel(q, k, v, g, 0)
+    assert rb.last_kernel() == parallel_tc_name(dk, dv, N, gated)
+    assert rb.parallel_format_reruns() > 0
+    for h in range(H):
+        sl = (slice(None), slice(None), slice(h * dv, (h + 1) * dv)) if gated else (slice(None), h)
+        assert err_bf16(got[sl], want[sl]) < TOL_BF16, h
+    rb.check_device_error()
