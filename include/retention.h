@@ -97,9 +97,10 @@ int retention_parallel(const void* q, const void* k, const void* v, void* o,
  * token before chunk i exactly, so every chunk length gives the same O and final state up
  * to rounding.  bf16 inputs run on the pair-of-SMs tensor-core kernel with 256-token
  * chunks whenever it applies (dk 256, dv a multiple of 128, N a multiple of 256, every
- * gamma^(-256) <= 2^64), whatever the caller's chunk; otherwise with the caller's chunk,
- * and a chunk below 128 (no tensor-core schedule of its own) with 128-token chunks when N
- * splits into them and the decays allow it (retention_last_kernel names the kernel).
+ * gamma^(-256) <= 2^64), whatever the caller's chunk; otherwise with the caller's chunk;
+ * otherwise with 128-token chunks when N splits into them and every gamma^(-128) <= 2^64
+ * (a chunk below 128 has no tensor-core schedule of its own); otherwise on CUDA cores
+ * (retention_last_kernel names the kernel).
  * fp32 inputs and every other case use the caller's chunk.
  */
 int retention_chunkwise(const void* q, const void* k, const void* v, void* o,

@@ -165,14 +165,14 @@ int retention_chunkwise(const void* q, const void* k, const void* v, void* o,
         // eq.(7) gives the same function for every chunk length (the chunk only orders the
         // work: R_i carries everything before the chunk exactly), so the call runs on the
         // fastest schedule that applies: the pair kernel with 256-token chunks when N splits
-        // into them, else the caller's chunk length (pair kernel, then one-SM kernel); a
-        // chunk below 128 has no tensor-core schedule of its own and runs with 256- or
-        // 128-token chunks when N splits into them, on the CUDA-core kernel otherwise.
+        // into them, else the caller's chunk length (pair kernel, then one-SM kernel), else
+        // 256- or 128-token chunks -- a chunk below 128 has no tensor-core schedule of its
+        // own, and decays too small for the folded factors at 256 tokens (g^-256 > 2^64)
+        // still fit them at 128 -- and the CUDA-core kernel when none applies.
         const int schedule[4] = {256, chunk, 256, 128};
         for (int i = 0; i < 4; ++i) {
             const int cb = schedule[i];
-            if (N % cb != 0 || (i == 0 && cb == chunk)) continue;
-            if (i >= 2 && chunk >= 128) continue;
+            if (N % cb != 0 || (i == 0 && cb == chunk) || (i >= 2 && cb == chunk)) continue;
             HeadConsts hcb;
             if (head_consts(gamma, H, cb, &hcb) != RET_OK) continue;
             cudaError_t e = ret::launch_chunkwise_tc_pair(q, k, v, o, ob, b, H, N, dk, dv, cb,

@@ -127,14 +127,18 @@ def test_tc_chunkwise_nonzero_state_in():
     assert err_f32(so, s_end) < TOL_BF16
 
 
-@pytest.mark.parametrize("chunk,gmin", [(128, 0.70), (256, 0.84)])
-def test_small_decay_uses_cuda_core_kernel(chunk, gmin):
-    """gamma^(-chunk) above 2^64 falls outside the folded-factor range: CUDA-core kernel."""
+@pytest.mark.parametrize("chunk,gmin,kernel", [(128, 0.70, "chunkwise_simt"),
+                                              (256, 0.70, "chunkwise_simt"),
+                                              (256, 0.84, "chunkwise_tc")])
+def test_small_decay_schedule(chunk, gmin, kernel):
+    """gamma^(-256) above 2^64 leaves the folded-factor range at 256-token chunks; 128-token
+    chunks on the one-SM kernel still hold it down to gamma ~ 0.71 (the same function), and
+    below that the CUDA-core kernel takes the call."""
     b, H, N, dk, dv = 1, 2, 512, 128, 64
     q, k, v = mk(b, H, N, dk, dv, 600)
     g = [gmin, 0.9]
     got = rb.retention_chunkwise(q, k, v, g, chunk)
-    assert rb.last_kernel() == "chunkwise_simt"
+    assert rb.last_kernel() == kernel
     assert err_bf16(got, oracle.chunkwise(q, k, v, g, chunk)) < TOL_BF16
 
 
