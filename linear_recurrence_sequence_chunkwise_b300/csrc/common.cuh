@@ -108,7 +108,9 @@ cudaError_t launch_chunkwise_tc(const void* q, const void* k, const void* v, voi
 // column slices of wider matrices are read and written in place.  rev != 0 runs eq.(7) in
 // reversed time on the rows as stored (row n collects the keys m >= n with g^(m-n); the
 // chunks are scanned from the last; state_in enters at the end, state_out leaves at the
-// start).  acc (fp32, pitch ldo, may equal o when o is fp32) is added to the output.
+// start).  acc (fp32) is added to the output: with fp32 output it must be o itself (the
+// kernel adds its rows to o by reductions in L2); with bf16 output it is a separate array of
+// pitch ldo.
 cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v, void* o,
                                      int out_bf16, int b, int H, int N, int dk, int dv, int chunk,
                                      const HeadConsts& hc, const float* state_in, float* state_out,

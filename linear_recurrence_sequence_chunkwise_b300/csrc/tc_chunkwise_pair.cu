@@ -456,8 +456,10 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 // of 16 bytes) is transposed within 8-lane groups (8 consecutive rows), so
                 // that every store instruction writes four whole 128-byte segments.  The last
                 // TMEM read releases O for the next Q.R.
-                // acc (optional, fp32, pitch ldo): added to the output (in place when acc is
-                // the output); each thread reads its own row's columns before the transpose.
+                // acc (optional): with fp32 output acc is the output itself, which already
+                // holds the earlier terms, and the rows are added to it by reductions in L2
+                // (no read on the SM); with bf16 output acc is a separate fp32 array (pitch
+                // ldo) that each thread reads for its own row's columns before the transpose.
                 auto row_of = [&](int c) {
                     return (size_t)bh * N + (size_t)(rev ? nchunks - 1 - c : c) * kB;
                 };
@@ -512,18 +514,10 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                             tmem_ld32(tc0, o);
                             tmem_wait_ld();
                             if (sg == kSegs - 1) { tc_fence_before(); arrive_lead(&bars.o_free); }
-                            if (ACC) {
-                                add_acc(o, c, colh + kSegCols * sg);
 #pragma unroll
-                                for (int k = 0; k < 8; ++k)
+                            for (int k = 0; k < 8; ++k)
 #pragma unroll
-                                    for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(o[4 * k + w]);
-                            } else {
-#pragma unroll
-                                for (int k = 0; k < 8; ++k)
-#pragma unroll
-                                    for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
-                            }
+                                for (int w = 0; w < 4; ++w) a[k][w] = __float_as_uint(xi * o[4 * k + w]);
                         }
                         transpose8x8(a, p8);
                         const size_t col = (size_t)blk * 128 + (size_t)(64 * half + kSegCols * sg);
@@ -536,7 +530,10 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                             else
                                 dst = reinterpret_cast<uint4*>(static_cast<float*>(out_base) +
                                                                (row0 + k) * ldo + col) + p8;
-                            *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
+                            if (ACC && !OUT_BF16)
+                                red_add_v4(reinterpret_cast<float*>(dst), a[k][0], a[k][1], a[k][2], a[k][3]);
+                            else
+                                *dst = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
                         }
                     }
                 };
@@ -604,7 +601,7 @@ chunkwise_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_const
                 };
                 for (int c = 0; c < nchunks && ok; ++c) {
                     // the rows acc adds to this chunk's output, into L2 ahead of use
-                    if (ACC) {
+                    if (ACC && OUT_BF16) {
                         const float* ar = acc + (row_of(c) + j) * ldo + blk * 128 + 64 * half;
                         prefetch_l2(ar);
                         prefetch_l2(ar + 32);
@@ -853,6 +850,8 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (acc && (reinterpret_cast<uintptr_t>(acc) & 15u)) return cudaErrorInvalidValue;
+    // fp32 output accumulates in place (the kernel adds to o and never reads acc)
+    if (acc && !out_bf16 && acc != o) return cudaErrorInvalidValue;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, o, state_in, state_out, N, H, dv,
                                                 fp16_first, dc, wait_ns, no_loads, ldo, acc);
     e = cudaGetLastError();
