@@ -830,6 +830,9 @@ cudaError_t launch_chunkwise_tc_pair(const void* q, const void* k, const void* v
         // stays in range only while g^(-B) <= 4096
         if (!(hc.l2g[h] * (float)chunk >= -12.0f)) fp16_first = 0;
     }
+    // An fp32 output that accumulates in place takes the hi/lo format from the start: a
+    // re-run would add the unit's rows to the output a second time.
+    if (acc && !out_bf16) fp16_first = 0;
     const long long rows = (long long)b * H * N;
     if (rows >= (1LL << 31)) return cudaErrorNotSupported;
     CUtensorMap mq, mk, mv;

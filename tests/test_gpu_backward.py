@@ -180,3 +180,28 @@ def test_tensor_core_passes_match_the_cuda_core_kernel_and_bf16_grads():
         assert g.dtype == torch.bfloat16
         assert err_bf16_out(g, w) <= 1.0
     rb.check_device_error()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_tensor_core_passes_with_operands_beyond_fp16(out_dtype):
+    """dout of head 0 scaled by 2^20 (|dout| up to ~2^18): the passes that read dout as Q,
+    as keys or as values leave fp16's range and run their units in the hi/lo format.  The
+    second half of dq and dk adds to the first half's output, so a re-run must not add twice.
+    The gradient is linear in dout: each head is compared with the oracle at its own scale."""
+    b, H, N, dk, dv = 1, 2, 512, 256, 512
+    gamma = [0.97, 0.995]
+    q, k, v, do, s0, ds = make(b, H, N, dk, dv, 900, "bf16", 1 / 16)
+    do[:, 0] *= 2.0 ** 20
+    rb.chunkwise_format_reruns()
+    got = run(q, k, v, do, gamma, 64, s0, ds, out_dtype=out_dtype)
+    reruns = rb.chunkwise_format_reruns()
+    assert reruns > 0
+    want = oracle.chunkwise_backward(q, k, v, do, gamma, state_in=s0, dstate_out=ds)
+    for name, g, w in zip(("dq", "dk", "dv", "dstate_in"), got, want):
+        for h in range(H):
+            gh, wh = g[:, h:h + 1], np.asarray(w)[:, h:h + 1]
+            if out_dtype == torch.bfloat16 and name != "dstate_in":
+                assert err_bf16_out(gh, wh) <= 1.0, (name, h)
+            else:
+                assert err_bf16(gh, wh) < TOL_BF16, (name, h)
+    rb.check_device_error()
