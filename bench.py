@@ -38,7 +38,8 @@ sys.path.insert(0, ROOT)
 from linear_recurrence_sequence_chunkwise_b300 import inputs  # noqa: E402
 
 METRIC = ("retention fwd tokens/s & % tensor peak (chunkwise); decode tokens/s & HBM GB/s")
-E2E_SEGMENT = 4096          # tokens per streamed segment of the end-to-end leg
+E2E_SEGMENT = 2048          # tokens per streamed segment of the end-to-end leg (1024: 30.8 ms,
+                            # 2048: 30.2, 4096: 30.4, 8192: 31.4 on chunkwise_long)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
