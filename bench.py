@@ -576,7 +576,8 @@ def bench_msr_layer(args, dist, rb, pk):
         rb.retention_msr_layer(x, *ws, gam, theta, flags=7, out=out, workspace=wsb)
 
     steps = max(3, args.steps // 5)
-    ms, _ = timed(step, steps, 3, dist)
+    with Clocks(torch.cuda.current_device()) as clk:
+        ms, _ = timed(step, steps, 3, dist)
     rb.check_device_error()
     ms_step = ms / steps
     value, _ = aggregate(dist, ms, b * N * steps)
@@ -595,7 +596,16 @@ def bench_msr_layer(args, dist, rb, pk):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
                          "algorithmic_flops_per_launch": flops,
-                         "flops_split": {"projections": proj, "retention_core": core}}}
+                         "flops_split": {"projections": proj, "retention_core": core},
+                         **sustained_frac(achieved, pk)},
+            "clocks": clk.summary()}
+
+
+def sustained_frac(achieved: float, pk: dict) -> dict:
+    """A dense tensor-core loop that runs long enough meets the board's power cap: the
+    fraction of the sustained peak (a seconds-long cuBLAS loop) beside the burst one."""
+    s = pk.get("bf16_tflops_sustained")
+    return {"peak_sustained": s, "frac_of_sustained": achieved / s} if s else {}
 
 
 def bench_gemm(args, dist, rb, pk):
@@ -605,7 +615,8 @@ def bench_gemm(args, dist, rb, pk):
     w = inputs.randn((K, Nc), 8101, K ** -0.5, "bf16", "cuda")
     c = torch.empty(M, Nc, dtype=torch.bfloat16, device="cuda")
     steps = max(3, args.steps // 2)
-    ms, _ = timed(lambda: rb.retention_gemm(a, w, out=c), steps, 3, dist)
+    with Clocks(torch.cuda.current_device()) as clk:
+        ms, _ = timed(lambda: rb.retention_gemm(a, w, out=c), steps, 3, dist)
     rb.check_device_error()
     ms_step = ms / steps
     flops = 2.0 * M * Nc * K
@@ -619,7 +630,8 @@ def bench_gemm(args, dist, rb, pk):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                          "traffic": profile_traffic("gemm_kernel_gemm.md", "tc_gemm.cu"),
-                         "algorithmic_flops_per_launch": flops}}
+                         "algorithmic_flops_per_launch": flops, **sustained_frac(achieved, pk)},
+            "clocks": clk.summary()}
 
 
 def cpu_baseline_leg():
