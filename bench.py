@@ -385,7 +385,8 @@ def bench_parallel(args, dist, rb, pk):
         rb.retention_parallel_gated(q, k, v, g, w.gamma, w.flags, w.eps, out=out)
 
     steps = max(3, args.steps // 2)
-    ms, _ = timed(step, steps, max(1, args.warmup // 2), dist)
+    with Clocks(torch.cuda.current_device()) as clk:
+        ms, _ = timed(step, steps, max(1, args.warmup // 2), dist)
     rb.check_device_error()
     ms_step = ms / steps
     tokens = w.b * w.N
@@ -402,7 +403,8 @@ def bench_parallel(args, dist, rb, pk):
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                          "traffic": profile_traffic(f"parallel_pair_{w.name}.md", "tc_parallel_pair.cu",
                                                     "tc_parallel.cu"),
-                         "algorithmic_flops_per_launch": flops}}
+                         "algorithmic_flops_per_launch": flops, **sustained_frac(achieved, pk)},
+            "clocks": clk.summary()}
 
 
 def bench_backward(args, dist, rb, pk):
@@ -424,7 +426,8 @@ def bench_backward(args, dist, rb, pk):
                                         cuda_cores=True)
 
     steps = max(3, args.steps // 4)
-    ms, _ = timed(step, steps, 3, dist)
+    with Clocks(torch.cuda.current_device()) as clk:
+        ms, _ = timed(step, steps, 3, dist)
     rb.check_device_error()
     ms_step = ms / steps
     ms_cc, _ = timed(step_cuda_cores, 3, 1, dist)
@@ -442,7 +445,8 @@ def bench_backward(args, dist, rb, pk):
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                          "traffic": profile_traffic("chunkwise_backward_tc_backward.md",
                                                     "backward_tc.cu", "tc_chunkwise_pair.cu"),
-                         "algorithmic_flops_per_launch": flops},
+                         "algorithmic_flops_per_launch": flops, **sustained_frac(achieved, pk)},
+            "clocks": clk.summary(),
             "cuda_core_kernel_ms_per_step": ms_cc / 3}
 
 
